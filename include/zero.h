@@ -1,0 +1,304 @@
+/*
+ * zero.h — C ABI of libzero: the ZeRO-DP partitioned mixed-precision AdamW
+ * step on one GB300 (sm_103a), with N_d simulated data-parallel ranks held as
+ * separate device buffers.
+ *
+ * One step (ZeRO-1/2): reduce-scatter the N_d 16-bit gradient replicas over a
+ * flat, padded, bucketed parameter buffer; compute the global gradient norm
+ * from every rank's partial sums; apply AdamW to each rank's fp32
+ * master/m/v shard; cast to 16 bits and all-gather into every rank's full
+ * parameter replica.  ZeRO-3 instead gathers the 16-bit shards of one unit
+ * (a transformer block, or the root unit with embeddings and head) into a
+ * transient buffer before forward and again before backward, reduce-scatters
+ * per unit and writes only the rank's 16-bit shard (no all-gather at the end
+ * of the step).
+ *
+ * Sources, by page title and section:
+ *   [L5]  "第 5 课：ZeRO 与 FSDP" (hsthanb4.github.io, hpclearning lesson 5):
+ *         §2 memory formulas, §3 reduce-scatter / update / all-gather and the
+ *         2Psi vs 3Psi volumes, Fig. 5-1 per-layer gather-and-release.
+ *   [RN]  "ZeRO: Memory Optimizations Toward Training Trillion Parameter
+ *         Models" (reading notes, unpurerationalist.github.io): §2.1 mixed
+ *         precision (fp32 master, m, v), §2.2 fp32 fused buffers, §3.1 dynamic
+ *         communication schedule, §4.1-§4.3 P_os / P_g / P_p, §5.2 constant
+ *         size buffers, §6 communication volumes.
+ *   [Z3]  "ZeRO-3 核心流程：把参数也切开的那一档" (llmnex.top): §2 the four actions
+ *         per layer, 坑 1 sharding-aware gradient clipping.
+ *   [FS]  "別再複製本可分片的東西：ZeRO 與 FSDP" (jovanaeducation.com): FSDP units.
+ *   [ML]  mlqm.cn data-parallel / ZeRO post: gradient buckets, ds_config.
+ * Where the pages are silent (AdamW formula, padding, bucket boundaries,
+ * rounding, loss scaling, overflow skip) the readings are stated at the
+ * function that uses them.
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller allocates and owns every device buffer (master,
+ *     m, v, replicas, shards, transients, workspace, state).  The library
+ *     never allocates device memory and never frees a caller pointer.  Only
+ *     the zero_layout object is library-owned (zero_layout_destroy frees it).
+ *   - Pointer arrays (`... const* x`) are HOST arrays of N_d DEVICE pointers,
+ *     one per simulated rank, read during the call only.
+ *   - Alignment: every device buffer must start on a 256-byte boundary, else
+ *     ZERO_ERR_ALIGN.  NULL where a buffer is required: ZERO_ERR_INVALID.
+ *   - Asynchrony: device calls enqueue kernels on `stream` and return without
+ *     synchronising the host.  A launch error returns ZERO_ERR_CUDA; a fault
+ *     during execution surfaces at the caller's next synchronisation.
+ *   - Status: no exception or abort crosses the ABI; the return value is the
+ *     only channel.  zero_last_error() gives a message for the last failing
+ *     call on the calling thread.
+ *   - Layout constants: q = N_d * 128 (or pad_multiple); Psi_pad = padded
+ *     flat length; S = per-rank shard length.  Rank r owns flat range
+ *     [r*S, (r+1)*S) for ZeRO-1/2, and slice [r*S_u, (r+1)*S_u) of every unit u
+ *     for ZeRO-3 (its shard is those slices concatenated in unit order).
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* zero_stream_t;
+
+typedef int32_t zero_status_t;
+enum {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID = -1, /* bad argument, size, index, stage or NULL pointer */
+    ZERO_ERR_ALIGN = -2,   /* a device buffer is not 256-byte aligned        */
+    ZERO_ERR_CUDA = -3,    /* a CUDA launch or query failed                  */
+    ZERO_ERR_STATE = -4,   /* call not valid for this layout's stage          */
+    ZERO_ERR_TIMEOUT = -5, /* reserved: no call waits on the device           */
+    ZERO_ERR_NOMEM = -6    /* host allocation of the layout object failed     */
+};
+
+typedef enum { ZERO_BF16 = 0, ZERO_FP16 = 1 } zero_dtype_t;
+
+#define ZERO_MAX_RANKS 64
+
+/* Output kinds of zero_adamw_shard_step / zero_fused_step. */
+enum {
+    ZERO_OUT_FULL_REPLICAS = 0, /* ZeRO-1/2: write each updated 16-bit value into
+                                   all N_d full replicas (all-gather fused)     */
+    ZERO_OUT_SHARDS = 1         /* write rank r's 16-bit shard only (ZeRO-3, or
+                                   ZeRO-1/2 followed by zero_allgather_params)  */
+};
+
+/* Flags of zero_grad_norm. */
+enum {
+    ZERO_NORM_DECIDE = 0,      /* split step: decide skip/clip before the update */
+    ZERO_NORM_AFTER_FUSED = 1  /* fused step: the update already ran; record the
+                                  norm and advance the step counter            */
+};
+
+typedef struct zero_layout zero_layout; /* opaque, immutable after init */
+
+/* Everything zero_layout_query reports.  Bytes are per rank; counters are
+ * elements moved per rank per step. */
+typedef struct zero_layout_info {
+    int32_t n_d, stage, dtype, n_tensors;
+    int32_t n_buckets, n_units, reserved0, reserved1;
+    int64_t psi;             /* real parameter count                          */
+    int64_t psi_pad;         /* padded flat length                            */
+    int64_t q;               /* padding quantum                               */
+    int64_t bucket_elems;    /* requested bucket size (<= 0: one bucket)      */
+    int64_t shard_len;       /* S: per-rank shard length (sum of S_u)         */
+    int64_t max_unit_padded; /* largest padded segment                        */
+    /* memory per rank, [L5] §2 M0..M3 with Psi -> Psi_pad and Psi/N_d -> S */
+    int64_t mem_formula;     /* M_stage                                       */
+    int64_t mem_state;       /* fp32 master + m + v shard: 12 S               */
+    int64_t mem_gshard;      /* fp32 reduced-gradient shard: 4 S ([RN] §2.2)   */
+    int64_t mem_transient;   /* ZeRO-3: 2 bytes x largest padded unit, else 0  */
+    int64_t mem_peak;        /* mem_formula + mem_transient                   */
+    /* communication per rank, [L5] §3 / [RN] §6: (N_d - 1) * S per collective */
+    int64_t comm_rs, comm_ag, comm_ag_fwd, comm_ag_bwd, comm_allreduce, comm_total;
+    int64_t workspace_bytes; /* device workspace the step calls need          */
+} zero_layout_info;
+
+/* One separately padded segment: the whole buffer for ZeRO-0/1/2, a unit for
+ * ZeRO-3. */
+typedef struct zero_unit_info {
+    int64_t offset;     /* flat offset                                        */
+    int64_t real;       /* real element count                                 */
+    int64_t padded;     /* padded element count (multiple of q)              */
+    int64_t shard;      /* S_u = padded / N_d                                 */
+    int64_t shard_base; /* offset of this segment inside every rank's shard  */
+} zero_unit_info;
+
+/* Device-resident step state (96 bytes).  Create it with zero_state_init;
+ * only the library's kernels write it afterwards.  The host may read it
+ * (after synchronising) to see the norm, the overflow flag and the counters. */
+typedef struct zero_step_state {
+    double beta1, beta2;         /* AdamW betas                                 */
+    double beta1_pow, beta2_pow; /* beta^t after t applied steps (t products)   */
+    double grad_norm;            /* global norm of the last step (+inf: overflow) */
+    float loss_scale;            /* current loss scale                          */
+    float clip_coef;             /* clip coefficient of the last step (1: none) */
+    int32_t t;                   /* applied (not skipped) steps                 */
+    int32_t skipped;             /* skipped steps                               */
+    int32_t good_steps;          /* applied steps since the last scale change   */
+    int32_t growth_interval;     /* double the scale after this many good steps */
+    int32_t dynamic_scale;       /* 1: halve on overflow, grow after interval   */
+    int32_t nonfinite;           /* OR of this step's reduce-scatter checks     */
+    int32_t overflow;            /* last decided step overflowed                */
+    int32_t apply;               /* last decided step applies the update        */
+    int32_t error;               /* device-detected error (0 = none)            */
+    int32_t reserved[3];
+} zero_step_state;
+
+/* AdamW hyperparameters that may change between steps (lr schedules).  The
+ * betas live in zero_step_state. */
+typedef struct zero_adamw_hp {
+    double lr;
+    double eps;
+    double weight_decay;
+} zero_adamw_hp;
+
+/* ------------------------------------------------------------------------ */
+/* Layout (host only, integer work)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Flatten, pad, shard, bucket and account ([RN] §2.2 and §5.2 flatten into one
+ * contiguous buffer; [L5] §2 and [RN] §4 equal 1/N_d split; [ML] "梯度桶化" and
+ * [RN] §4.1-§4.2 fixed-size buckets; [FS] one unit per block plus a root unit).
+ *   numels[n_tensors]   element count of each tensor, declaration order (> 0).
+ *   unit_of_tensor      ZeRO-3 unit id per tensor (0..U-1, none empty), or
+ *                       NULL for stages 0-2 (required for stage 3).
+ *   n_d                 simulated ranks, 1..ZERO_MAX_RANKS.
+ *   stage               0 (DDP: accounting only), 1, 2 or 3.
+ *   pad_multiple        0 => q = n_d*128; else a positive multiple of n_d*128.
+ *   bucket_elems        <= 0: one bucket; else a multiple of 32.  Buckets are
+ *                       [k*B, min((k+1)*B, Psi_pad)); ZeRO-3 buckets are units.
+ *   dtype               16-bit format of gradients and parameters.
+ * Readings: stages 0-2 flatten in declaration order with no gaps and pad the
+ * tail with zeros to a multiple of q; stage 3 lays units out in id order, each
+ * unit's tensors in declaration order, each unit padded to a multiple of q.
+ * On success *out owns a new layout; on error *out is untouched. */
+zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tensors,
+                               const int32_t* unit_of_tensor, int32_t n_d, int32_t stage,
+                               int64_t pad_multiple, int64_t bucket_elems,
+                               zero_dtype_t dtype, zero_layout** out);
+zero_status_t zero_layout_query(const zero_layout* L, zero_layout_info* out);
+/* [begin, end) of bucket b (ZeRO-3: of unit b). */
+zero_status_t zero_layout_bucket(const zero_layout* L, int32_t b, int64_t* begin, int64_t* end);
+zero_status_t zero_layout_unit(const zero_layout* L, int32_t u, zero_unit_info* out);
+/* Flat offset of tensor t. */
+zero_status_t zero_layout_tensor_offset(const zero_layout* L, int32_t t, int64_t* offset);
+void zero_layout_destroy(zero_layout* L);
+
+/* ------------------------------------------------------------------------ */
+/* Step state                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Write the initial state into device memory `st` (t = 0, betas, beta^0 = 1,
+ * loss_scale >= 1, no error).  growth_interval >= 1.  One tiny kernel. */
+zero_status_t zero_state_init(zero_step_state* st, double beta1, double beta2,
+                              float loss_scale, int32_t dynamic_scale,
+                              int32_t growth_interval, zero_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* The step                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Reduce-scatter of one bucket (ZeRO-1/2) or one unit (ZeRO-3) ([L5] §3 step
+ * 1; [RN] §4.1-§4.3 bucketed, asynchronous reduce-scatter; [Z3] §2 backward).
+ * For every flat index i of the bucket, owned by rank r at shard offset j:
+ *   s = x_0 + x_1 + ... + x_{N_d-1}   (x_k = grad_replicas[k][i], binary32
+ *                                      adds in rank order; padding reads 0)
+ *   grad_shards[r][j] = s / (N_d * loss_scale)   (IEEE division)
+ * It also writes the 32-element sums of squares used by zero_grad_norm into
+ * `workspace` and ORs "some s is inf/NaN" into st->nonfinite.
+ *   grad_replicas: N_d device pointers to full 16-bit replicas (Psi_pad each).
+ *   grad_shards:   N_d device pointers to fp32 shards (S each).
+ *   workspace:     >= info.workspace_bytes, shared by all calls of a step.
+ * Every bucket (unit) must be reduced once per step before zero_grad_norm.
+ * Stage 0: ZERO_ERR_STATE. */
+zero_status_t zero_reduce_scatter(const zero_layout* L, int32_t bucket_or_unit,
+                                  const void* const* grad_replicas, float* const* grad_shards,
+                                  zero_step_state* st, void* workspace, zero_stream_t stream);
+
+/* Sharding-aware global gradient norm and the step decision ([Z3] 坑 1: the
+ * norm must combine every shard's partial sums, else each rank clips by a
+ * different coefficient).  Two deterministic passes over the 32-element
+ * partials (binary64 from there on): norm = sqrt(sum g^2) over all Psi_pad.
+ * ZERO_NORM_DECIDE (split step, before zero_adamw_shard_step):
+ *   overflow = st->nonfinite.  If overflow: grad_norm = +inf, the update is
+ *   skipped (apply = 0), skipped += 1, a dynamic scale halves (never below 1).
+ *   Else: clip_coef = min(1, max_norm / (norm + 1e-6)) (1 if max_norm <= 0),
+ *   t += 1, beta^t advance, apply = 1, and a dynamic scale doubles after
+ *   growth_interval consecutive applied steps.
+ * ZERO_NORM_AFTER_FUSED (after zero_fused_step): records the norm and the
+ *   overflow flag, and advances t and beta^t (the update already ran).
+ * Both clear st->nonfinite for the next step.  Readings: the skip rule, the
+ * 1e-6 and the scale schedule are not on the pages (mixed-precision practice). */
+zero_status_t zero_grad_norm(const zero_layout* L, double max_norm, int32_t flags,
+                             zero_step_state* st, void* workspace, zero_stream_t stream);
+
+/* Sharded AdamW, cast and (optionally fused) all-gather ([L5] §3 step 2: each
+ * rank updates its 1/N_d fp32 state and casts it to 16 bits in place; [RN]
+ * §4.1 then all-gathers; [Z3] §2 step 3 zero communication).  No-op when
+ * st->apply == 0.  Per element of every rank's shard, one binary32 rounding
+ * per operation, no fused multiply-add (reading: decoupled weight decay):
+ *   g'  = g * clip_coef
+ *   p1  = p * (1 - lr*wd)
+ *   m   = beta1*m + (1-beta1)*g'
+ *   v   = beta2*v + (1-beta2)*(g'*g')
+ *   den = sqrt(v) / sqrt(1 - beta2^t) + eps
+ *   p   = p1 - (lr / (1 - beta1^t)) * (m / den)
+ *   out = round-to-nearest-even 16-bit(p)
+ * Constants are computed in binary64 and rounded once to binary32.
+ *   master, m, v:  N_d device pointers to fp32 shards (S each), updated in place.
+ *   grad_shards:   N_d fp32 shards written by zero_reduce_scatter.
+ *   param16_out:   ZERO_OUT_FULL_REPLICAS: N_d full 16-bit replicas (Psi_pad);
+ *                  ZERO_OUT_SHARDS: N_d 16-bit shards (S).  ZeRO-3 requires
+ *                  ZERO_OUT_SHARDS. */
+zero_status_t zero_adamw_shard_step(const zero_layout* L, const zero_adamw_hp* hp,
+                                    float* const* master, float* const* m, float* const* v,
+                                    const float* const* grad_shards, zero_step_state* st,
+                                    void* const* param16_out, int32_t out_kind,
+                                    zero_stream_t stream);
+
+/* Unfused all-gather of 16-bit shards into every rank's full replica
+ * (ZeRO-1/2; [L5] §3 step 3, [RN] §6.2.1): param16_full[k][r*S + j] =
+ * param16_shards[r][j] for every k, r, j.  Stage 3: ZERO_ERR_STATE. */
+zero_status_t zero_allgather_params(const zero_layout* L, const void* const* param16_shards,
+                                    void* const* param16_full, zero_stream_t stream);
+
+/* ZeRO-3 gather of unit `unit` into every rank's transient buffer ([L5]
+ * Fig. 5-1; [RN] §3.1 and §4.3; [Z3] §2 steps 1-2): transient[k][i] =
+ * param16_shards[r][S_u_base + i - r*S_u] for i in [0, real_u), r = i / S_u,
+ * for every rank k.  The unit's padding is not written.  "Release" is the
+ * caller reusing the buffer for the next unit.  transient: N_d device
+ * pointers, each >= real_u 16-bit elements.  Stages 0-2: ZERO_ERR_STATE. */
+zero_status_t zero_stage3_gather_layer(const zero_layout* L, int32_t unit,
+                                       const void* const* param16_shards, void* const* transient,
+                                       zero_stream_t stream);
+
+/* Reduce-scatter + AdamW + cast (+ all-gather) in one pass, for steps with
+ * neither clipping nor a loss scaler (the update cannot wait for a global
+ * norm): the arithmetic of zero_reduce_scatter and zero_adamw_shard_step per
+ * element, with clip_coef = 1 and the constants of step t + 1.  It also writes
+ * the norm partials and ORs st->nonfinite; follow it (after all buckets or
+ * units of the step) with zero_grad_norm(..., ZERO_NORM_AFTER_FUSED, ...).
+ * bucket_or_unit: a bucket (ZeRO-1/2) or unit (ZeRO-3) index, or -1 for the
+ * whole buffer.  Stage 1/2 with ZERO_OUT_FULL_REPLICAS or ZERO_OUT_SHARDS;
+ * stage 3 with ZERO_OUT_SHARDS.  A non-finite gradient is reported but not
+ * skipped (use the split calls when a loss scaler is active). */
+zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
+                              const zero_adamw_hp* hp, const void* const* grad_replicas,
+                              float* const* master, float* const* m, float* const* v,
+                              zero_step_state* st, void* const* param16_out, int32_t out_kind,
+                              void* workspace, zero_stream_t stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* zero_last_error(void);
+
+/* Number of device kernels the library launched on this thread since the
+ * last reset (for launch accounting in benchmarks). */
+int64_t zero_launch_count(int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

@@ -196,8 +196,11 @@ class StepState:
     def divisor(self, n_d: int) -> float:
         return _f32(n_d * self.loss_scale)
 
-    def decide(self, nonfinite: bool, sumsq: float, max_norm: float) -> Tuple[bool, float, float]:
-        """Returns (apply, norm, clip) and advances the state."""
+    def decide(self, nonfinite: bool, sumsq: float, max_norm: float,
+               clip_override: Optional[float] = None) -> Tuple[bool, float, float]:
+        """Returns (apply, norm, clip) and advances the state.  ``clip_override``
+        (tests only) replaces the computed coefficient, to separate the norm's
+        summation-order error from the update's arithmetic."""
         if nonfinite:
             norm, clip, apply = math.inf, 1.0, False
             self.skipped += 1
@@ -207,6 +210,8 @@ class StepState:
         else:
             norm = math.sqrt(sumsq)
             clip = _f32(min(1.0, max_norm / (norm + CLIP_EPS))) if max_norm > 0 else 1.0
+            if clip_override is not None:
+                clip = _f32(clip_override)
             apply = True
             self.t += 1
             self.good += 1
@@ -330,7 +335,7 @@ class ZeroSimulation:
         return sum_sequential(np.concatenate(parts))
 
     # -- one step --------------------------------------------------------------
-    def step(self, reps: Sequence[np.ndarray]) -> dict:
+    def step(self, reps: Sequence[np.ndarray], clip_override: Optional[float] = None) -> dict:
         L, st = self.L, self.state
         D = st.divisor(L.n_d)
         bad = False
@@ -351,7 +356,7 @@ class ZeroSimulation:
             for (b0, b1) in reversed(L.buckets):           # last bucket first
                 bad = self._reduce_scatter(b0, b1, reps, D) or bad
         sumsq = self._global_sumsq() if not bad else math.inf
-        apply, norm, clip = st.decide(bad, sumsq, self.max_norm)
+        apply, norm, clip = st.decide(bad, sumsq, self.max_norm, clip_override)
         if apply:
             for r in range(L.n_d):
                 adamw_inplace(self.master[r], self.m[r], self.v[r], self.gshard[r], self.hp, st.t, clip)

@@ -1,0 +1,147 @@
+"""C ABI checks that need no GPU: libzero.so loads, exports every entry point
+that include/zero.h declares, its host-side layout and accounting equal the
+oracle's bit for bit, and argument validation fails before any launch.
+
+Only argument errors that the library rejects before touching the device are
+exercised here (NULL, misaligned, out-of-range, wrong stage)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle.layout import layout_comm_elems, layout_memory_bytes, make_layout
+from zero_partitioned_mixed_replica_gb300 import binding as B
+from zero_partitioned_mixed_replica_gb300 import build as zbuild
+from zero_partitioned_mixed_replica_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    zbuild.build()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "zero.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert "zero_reduce_scatter" in names and "zero_stage3_gather_layer" in names
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.EXPORTED) == names
+
+
+def _layout_pair(numels, n_d, stage, bucket=0, units=None):
+    L = B.zero_layout_init(numels, units, n_d, stage, 0, bucket, B.ZERO_BF16)
+    O = make_layout(numels, n_d, stage, bucket_elems=bucket, unit_of_tensor=units)
+    return L, O
+
+
+CASES = [
+    ([1000 * 512, 512, 487 * 1000, 2491], 4, 2, 0, None),
+    ([3000, 17, 5000, 1], 3, 1, 640, None),
+    ([300, 2000, 64, 1500, 7], 5, 3, 0, [0, 1, 1, 2, 0]),
+    ([1], 1, 2, 32, None),
+    ([7, 9, 11], 64, 2, 96, None),
+    ([10, 20, 300, 5], 2, 3, 0, [1, 0, 1, 2]),
+    ([5, 6, 7], 8, 0, 0, None),
+]
+
+
+@pytest.mark.parametrize("numels,n_d,stage,bucket,units", CASES)
+def test_layout_matches_oracle(numels, n_d, stage, bucket, units):
+    L, O = _layout_pair(numels, n_d, stage, bucket, units)
+    info = B.zero_layout_query(L)
+    assert (info.psi, info.psi_pad, info.shard_len, info.q) == (O.psi, O.psi_pad, O.shard_len, O.q)
+    assert info.n_buckets == len(O.buckets) and info.n_units == len(O.units)
+    assert [B.zero_layout_bucket(L, b) for b in range(info.n_buckets)] == O.buckets
+    for u in range(info.n_units):
+        ui, ou = B.zero_layout_unit(L, u), O.units[u]
+        assert (ui.offset, ui.real, ui.padded, ui.shard, ui.shard_base) == \
+               (ou.offset, ou.real, ou.padded, ou.shard, ou.shard_base)
+    assert [B.zero_layout_tensor_offset(L, t) for t in range(len(numels))] == O.tensor_offsets
+    mem, comm = layout_memory_bytes(O), layout_comm_elems(O)
+    assert (info.mem_formula, info.mem_state, info.mem_gshard, info.mem_transient, info.mem_peak) == \
+           (mem["formula"], mem["state"], mem["gshard"], mem["transient"], mem["peak"])
+    assert (info.comm_rs, info.comm_ag, info.comm_ag_fwd, info.comm_ag_bwd, info.comm_allreduce,
+            info.comm_total) == (comm["rs"], comm["ag"], comm["ag_fwd"], comm["ag_bwd"], comm["allreduce"],
+                                 comm["total"])
+    assert info.workspace_bytes >= info.psi_pad // 32 * 4 + 1024 * 8
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_xl", "llama7b"])
+def test_workload_layouts_match_oracle(name):
+    w = workloads.ALL[name]()
+    units = w.unit_of_tensor if w.stage == 3 else None
+    L, O = _layout_pair(w.numels, w.n_d, w.stage, w.bucket_elems if w.stage != 3 else 0, units)
+    info = B.zero_layout_query(L)
+    assert (info.psi_pad, info.shard_len, info.n_buckets) == (O.psi_pad, O.shard_len, len(O.buckets))
+    assert [B.zero_layout_tensor_offset(L, t) for t in range(len(w.numels))] == O.tensor_offsets
+
+
+@pytest.mark.parametrize("args,status", [
+    (([], None, 2, 1, 0, 0, 0), B.ZERO_ERR_INVALID),
+    (([5], None, 0, 1, 0, 0, 0), B.ZERO_ERR_INVALID),
+    (([5], None, 65, 1, 0, 0, 0), B.ZERO_ERR_INVALID),
+    (([5], None, 2, 4, 0, 0, 0), B.ZERO_ERR_INVALID),
+    (([5], None, 2, 3, 0, 0, 0), B.ZERO_ERR_INVALID),          # stage 3 without units
+    (([5, 6], [0, 2], 2, 3, 0, 0, 0), B.ZERO_ERR_INVALID),      # empty unit 1
+    (([5], None, 2, 1, 100, 0, 0), B.ZERO_ERR_INVALID),         # pad not a multiple of n_d*128
+    (([5], None, 2, 1, 0, 48, 0), B.ZERO_ERR_INVALID),          # bucket not a multiple of 32
+    (([5], None, 2, 1, 0, 0, 7), B.ZERO_ERR_INVALID),           # dtype
+    (([0, 5], None, 2, 1, 0, 0, 0), B.ZERO_ERR_INVALID),        # empty tensor
+])
+def test_layout_init_rejects(args, status):
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_layout_init(*args)
+    assert e.value.status == status
+    assert B.zero_last_error()
+
+
+FAKE = 1 << 40          # 256-aligned host-side stand-in, never dereferenced: every
+MIS = FAKE + 16         # call below is rejected by validation before any launch
+
+
+def test_step_calls_validate_before_launch():
+    L = B.zero_layout_init([1000, 24], None, 2, 2, 0, 0, B.ZERO_BF16)
+    L3 = B.zero_layout_init([1000, 24], [0, 1], 2, 3, 0, 0, B.ZERO_BF16)
+    L0 = B.zero_layout_init([1000, 24], None, 2, 0, 0, 0, B.ZERO_BF16)
+    two = [FAKE, FAKE]
+    hp = B.zero_adamw_hp(lr=1e-3, eps=1e-8, weight_decay=0.0)
+
+    def status(fn, *a):
+        with pytest.raises(B.ZeroError) as e:
+            fn(*a)
+        return e.value.status
+
+    assert status(B.zero_reduce_scatter, L, 5, two, two, FAKE, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_reduce_scatter, L, 0, [FAKE, MIS], two, FAKE, FAKE, 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_reduce_scatter, L, 0, [FAKE, 0], two, FAKE, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_reduce_scatter, L, 0, two, two, MIS, FAKE, 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_reduce_scatter, L0, 0, two, two, FAKE, FAKE, 0) == B.ZERO_ERR_STATE
+    assert status(B.zero_grad_norm, L, 1.0, 7, FAKE, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_grad_norm, L, float("nan"), 0, FAKE, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_grad_norm, L, 1.0, 0, FAKE, 0, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_adamw_shard_step, L3, hp, two, two, two, two, FAKE, two,
+                  B.ZERO_OUT_FULL_REPLICAS, 0) == B.ZERO_ERR_STATE
+    assert status(B.zero_adamw_shard_step, L, hp, two, two, two, two, FAKE, two, 9, 0) == B.ZERO_ERR_INVALID
+    bad_hp = B.zero_adamw_hp(lr=1e-3, eps=0.0, weight_decay=0.0)
+    assert status(B.zero_adamw_shard_step, L, bad_hp, two, two, two, two, FAKE, two,
+                  B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_allgather_params, L3, two, two, 0) == B.ZERO_ERR_STATE
+    assert status(B.zero_stage3_gather_layer, L, 0, two, two, 0) == B.ZERO_ERR_STATE
+    assert status(B.zero_stage3_gather_layer, L3, 2, two, two, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_fused_step, L, 3, hp, two, two, two, two, FAKE, two,
+                  B.ZERO_OUT_FULL_REPLICAS, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_fused_step, L3, -1, hp, two, two, two, two, FAKE, two,
+                  B.ZERO_OUT_SHARDS, FAKE, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_state_init, MIS, 0.9, 0.999, 1.0, False, 10, 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_state_init, FAKE, 1.0, 0.999, 1.0, False, 10, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_state_init, FAKE, 0.9, 0.999, 0.5, False, 10, 0) == B.ZERO_ERR_INVALID

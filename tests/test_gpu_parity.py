@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element by
+element, on the same seeded inputs (drawn on the CPU, copied to the GPU).
+
+Sizes span many CTAs and grid-stride rounds with ragged tails (padding inside
+the last vector, buckets that straddle shards, units of different sizes).
+The bar: step flags, counters and loss scale bit-exact; fp32 master/m/v within
+1e-6 relative (|x| < 1e-30 absolutely within 1e-36); 16-bit parameters within
+1 ulp; the global norm within 1e-5 relative.  Bitwise equality of the state is
+also asserted wherever GPU and oracle used the same clip coefficient (always,
+when the oracle is re-run with the GPU's coefficient)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.step import AdamWHP, FMT_BF16, FMT_FP16, ZeroSimulation
+from tests._cases import Case
+
+pytestmark = pytest.mark.gpu
+
+HP = AdamWHP()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from zero_partitioned_mixed_replica_gb300 import build
+    build.build()
+
+
+def _engine(case: Case, **kw):
+    from zero_partitioned_mixed_replica_gb300.engine import AdamW, ZeroStep
+    return ZeroStep(case.numels, case.n_d, case.stage, case.fmt, case.bucket_elems, case.units,
+                    AdamW(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay), case.max_norm,
+                    case.loss_scale, case.dynamic, case.growth_interval, **kw)
+
+
+def _u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _ulp_key(h: np.ndarray) -> np.ndarray:
+    h = h.astype(np.int64)
+    return np.where(h & 0x8000, -(h & 0x7FFF), h)
+
+
+def assert_state_close(gpu: np.ndarray, ref: np.ndarray, what: str):
+    assert gpu.shape == ref.shape
+    d = np.abs(gpu.astype(np.float64) - ref.astype(np.float64))
+    big = np.abs(ref) >= 1e-30
+    bad = np.flatnonzero((big & (d > 1e-6 * np.abs(ref))) | (~big & (d > 1e-36)))
+    assert bad.size == 0, "%s: %d elements out of tolerance, e.g. idx %s gpu %s ref %s" % (
+        what, bad.size, bad[:3], gpu[bad[:3]], ref[bad[:3]])
+
+
+def assert_p16_close(gpu: np.ndarray, ref: np.ndarray, what: str):
+    dist = np.abs(_ulp_key(gpu) - _ulp_key(ref))
+    assert dist.max(initial=0) <= 1, "%s: max ulp distance %d" % (what, dist.max())
+
+
+def run_parity(case: Case, steps: int, garbage_pads: bool = False, use_gpu_clip: bool = False,
+               expect_bitwise: bool = True, **engine_kw):
+    L = case.layout()
+    eng = _engine(case, **engine_kw)
+    m0 = case.master0(L)
+    eng.load_master(torch.from_numpy(m0))
+    zs = ZeroSimulation(L, m0, case.fmt, HP, max_norm=case.max_norm, loss_scale=case.loss_scale,
+                        dynamic=case.dynamic, growth_interval=case.growth_interval)
+    pad = np.zeros(L.psi_pad, bool)
+    for u in L.units:
+        pad[u.offset + u.real:u.offset + u.padded] = True
+    hist = []
+    for s in range(1, steps + 1):
+        reps_t = case.grads_torch(L, s, zs.state.loss_scale)
+        reps = [_u16(t) for t in reps_t]
+        for r in range(case.n_d):
+            eng.grads[r].copy_(reps_t[r].to(eng.device))
+            if garbage_pads and pad.any():
+                idx = torch.from_numpy(np.flatnonzero(pad)).to(eng.device)
+                eng.grads[r].view(torch.int16)[idx] = 0x7F81 if r % 2 else 0x7C00   # NaN / inf bits
+        eng.step()
+        g = eng.read_state()
+        o = zs.step(reps, clip_override=g["clip_coef"] if use_gpu_clip else None)
+        hist.append((g, o))
+        assert g["overflow"] == o["overflow"], s
+        assert g["t"] == o["t"] and g["skipped"] == zs.state.skipped, s
+        assert g["loss_scale"] == o["loss_scale"], s
+        assert g["error"] == 0 and g["nonfinite"] == 0
+        if o["overflow"]:
+            assert math.isinf(g["grad_norm"])
+        else:
+            assert g["grad_norm"] == pytest.approx(o["norm"], rel=1e-5, abs=1e-30)
+            assert abs(g["grad_norm"] - o["norm"]) <= 1e-9 * o["norm"] + 1e-30  # aim: far inside the bar
+        same_clip = np.float32(g["clip_coef"]) == np.float32(o["clip"])
+        for name in ("master", "m", "v"):
+            gpu = eng.flat(name).cpu().numpy()
+            ref = zs.flat(name)
+            assert_state_close(gpu, ref, "%s step %d" % (name, s))
+            if expect_bitwise and same_clip:
+                assert np.array_equal(gpu.view(np.uint32), ref.view(np.uint32)), "%s step %d bitwise" % (name, s)
+            assert not gpu[pad].any(), "padding of %s must stay 0" % name
+        if case.stage == 3:
+            gp, rp = _u16(eng.flat("shard16")), zs.flat("shard16")
+            assert_p16_close(gp, rp, "shard16 step %d" % s)
+            if expect_bitwise and same_clip:
+                assert np.array_equal(gp, rp)
+        else:
+            for r in range(case.n_d):
+                gp = _u16(eng.params[r])
+                assert_p16_close(gp, zs.params16[r], "params16[%d] step %d" % (r, s))
+                if expect_bitwise and same_clip:
+                    assert np.array_equal(gp, zs.params16[r])
+    return eng, zs, hist
+
+
+def test_tiny_fused_zero2():
+    # Psi = 1,002,003 (4 tensors), N_d = 4, ZeRO-2, bf16, one bucket, 3 steps
+    c = Case([1000 * 512, 512, 487 * 1000, 2491], 4, 2, FMT_BF16)
+    run_parity(c, 3)
+
+
+def test_tiny_fused_per_bucket_equals_whole_buffer():
+    c = Case([1000 * 512, 512, 487 * 1000, 2491], 4, 2, FMT_BF16, bucket_elems=4096 * 7 + 32)
+    e1, _, _ = run_parity(c, 2, per_bucket=True)
+    e2, _, _ = run_parity(c, 2, per_bucket=False)
+    assert torch.equal(e1.master, e2.master) and torch.equal(e1.params, e2.params)
+
+
+@pytest.mark.parametrize("n_d", [1, 2, 3, 5, 8, 16])
+def test_zero1_fused_all_rank_counts(n_d):
+    c = Case([40_000, 33, 77_777, 5], n_d, 1, FMT_BF16, bucket_elems=65_536, per_tensor_scale=True)
+    run_parity(c, 2)
+
+
+@pytest.mark.parametrize("n_d", [2, 3, 8])
+def test_zero2_split_clip_bf16(n_d):
+    c = Case([120_000, 7, 50_001], n_d, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05,
+             per_tensor_scale=True)
+    _, _, hist = run_parity(c, 3, use_gpu_clip=True)
+    assert all(g["clip_coef"] < 1.0 for g, _ in hist)
+
+
+def test_zero2_split_clip_independent_coefficient():
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05, per_tensor_scale=True)
+    run_parity(c, 3, use_gpu_clip=False)
+
+
+def test_zero2_fp16_scaler_overflow_skip():
+    # like the GPT-2 1.5B run: fp16 grads x 2^16, dynamic scale, clip 1.0, +inf in rank 3 at step 4
+    c = Case([200_000, 1600, 99_999], 8, 2, FMT_FP16, bucket_elems=65_536, max_norm=1.0,
+             loss_scale=65536.0, dynamic=True, per_tensor_scale=True, inf_step=4, inf_rank=3)
+    eng, zs, hist = run_parity(c, 6, use_gpu_clip=True)
+    assert [g["overflow"] for g, _ in hist] == [0, 0, 0, 1, 0, 0]
+    assert [g["loss_scale"] for g, _ in hist] == [65536.0] * 3 + [32768.0] * 3
+    assert [g["t"] for g, _ in hist] == [1, 2, 3, 3, 4, 5]
+
+
+def test_scale_growth_on_gpu():
+    c = Case([30_000], 2, 2, FMT_FP16, loss_scale=256.0, dynamic=True, growth_interval=2)
+    _, _, hist = run_parity(c, 5)
+    assert [g["loss_scale"] for g, _ in hist] == [256.0, 512.0, 512.0, 1024.0, 1024.0]
+
+
+def test_garbage_in_gradient_padding_is_ignored():
+    c = Case([1000 * 512, 512, 487 * 1000, 2491], 4, 2, FMT_BF16, max_norm=0.5)
+    run_parity(c, 2, garbage_pads=True, use_gpu_clip=True)
+    c = Case([100_001, 3], 3, 1, FMT_BF16)
+    run_parity(c, 2, garbage_pads=True)
+
+
+def test_unfused_allgather_equals_fused():
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    e1, _, _ = run_parity(c, 2, use_gpu_clip=True, fuse_allgather=False)
+    e2, _, _ = run_parity(c, 2, use_gpu_clip=True, fuse_allgather=True)
+    assert torch.equal(e1.params, e2.params) and torch.equal(e1.master, e2.master)
+
+
+def test_split_equals_fused_without_clip():
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768)
+    e1, _, _ = run_parity(c, 2, fused=False)
+    e2, _, _ = run_parity(c, 2, fused=True)
+    assert torch.equal(e1.master, e2.master) and torch.equal(e1.params, e2.params)
+
+
+Z3_NUMELS = [30_000, 60_000, 640, 45_000, 7, 20_000, 3]
+Z3_UNITS = [0, 1, 1, 2, 0, 3, 3]
+
+
+@pytest.mark.parametrize("n_d", [1, 2, 5])
+def test_zero3_fused_with_transients(n_d):
+    c = Case(Z3_NUMELS, n_d, 3, FMT_BF16, units=Z3_UNITS)
+    L = c.layout()
+    seen = []
+
+    def hook(kind, u, rows):
+        torch.cuda.synchronize()
+        unit = L.units[u]
+        seen.append((kind, u, [_u16(r[:unit.real]) for r in rows]))
+
+    eng = _engine(c)
+    eng.transient_hook = hook
+    m0 = c.master0(L)
+    eng.load_master(torch.from_numpy(m0))
+    zs = ZeroSimulation(L, m0, c.fmt, HP)
+    zs.record_transients = True
+    for s in range(1, 4):
+        seen.clear()
+        reps_t = c.grads_torch(L, s, 1.0)
+        for r in range(n_d):
+            eng.grads[r].copy_(reps_t[r].cuda())
+        eng.step()
+        zs.step([_u16(t) for t in reps_t])
+        assert [(k, u) for k, u, _ in seen] == [(k, u) for k, u, _ in zs.transients]
+        for (k, u, gts), (_, _, ots) in zip(seen, zs.transients):
+            for a, b in zip(gts, ots):
+                assert np.array_equal(a, b), (k, u)
+        assert np.array_equal(_u16(eng.flat("shard16")), zs.flat("shard16"))
+        for name in ("master", "m", "v"):
+            assert np.array_equal(eng.flat(name).cpu().numpy().view(np.uint32), zs.flat(name).view(np.uint32))
+
+
+def test_zero3_split_fp16_clip_scaler():
+    c = Case(Z3_NUMELS, 4, 3, FMT_FP16, units=Z3_UNITS, max_norm=0.01, loss_scale=1024.0, dynamic=True,
+             inf_step=2, inf_rank=1)
+    _, _, hist = run_parity(c, 4, use_gpu_clip=True)
+    assert [g["overflow"] for g, _ in hist] == [0, 1, 0, 0]
+
+
+def test_zero3_garbage_pads():
+    c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS)
+    run_parity(c, 2, garbage_pads=True)
+
+
+def test_bucket_size_invariance_on_gpu():
+    outs = []
+    for bucket in (0, 32, 4096, 65_536 + 32):
+        c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=bucket, max_norm=0.05)
+        L = c.layout()
+        eng = _engine(c)
+        eng.load_master(torch.from_numpy(c.master0(L)))
+        for s in range(1, 3):
+            for r, t in enumerate(c.grads_torch(L, s, 1.0)):
+                eng.grads[r].copy_(t.cuda())
+            eng.step()
+        st = eng.read_state()
+        outs.append((st["grad_norm"], st["clip_coef"], eng.master.clone(), eng.params.clone()))
+    for o in outs[1:]:
+        assert o[0] == outs[0][0] and o[1] == outs[0][1]
+        assert torch.equal(o[2], outs[0][2]) and torch.equal(o[3], outs[0][3])
+
+
+def test_cuda_graph_replay_equals_eager():
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_FP16, bucket_elems=32_768, max_norm=1.0, loss_scale=65536.0,
+             dynamic=True)
+    L = c.layout()
+    res = []
+    for graph in (False, True):
+        eng = _engine(c)
+        eng.load_master(torch.from_numpy(c.master0(L)))
+        for r, t in enumerate(c.grads_torch(L, 1, 65536.0)):
+            eng.grads[r].copy_(t.cuda())
+        if graph:
+            g = eng.capture()
+            eng.reset_state()
+            eng.load_master(torch.from_numpy(c.master0(L)))
+            for _ in range(3):
+                g.replay()
+        else:
+            for _ in range(3):
+                eng.step()
+        res.append((eng.read_state(), eng.master.clone(), eng.params.clone()))
+    assert res[0][0]["t"] == res[1][0]["t"] == 3
+    assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+
+
+def test_deterministic_rerun():
+    c = Case([120_000, 7, 50_001], 8, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    a, _, ha = run_parity(c, 2, use_gpu_clip=True)
+    b, _, hb = run_parity(c, 2, use_gpu_clip=True)
+    assert [g["grad_norm"] for g, _ in ha] == [g["grad_norm"] for g, _ in hb]
+    assert torch.equal(a.master, b.master) and torch.equal(a.params, b.params)
+
+
+def test_launch_count_of_a_split_step():
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    eng = _engine(c)
+    Bd.zero_launch_count(reset=True)
+    eng.step()
+    torch.cuda.synchronize()
+    # one reduce-scatter per bucket, two norm passes, one AdamW
+    assert Bd.zero_launch_count() == eng.n_buckets + 3

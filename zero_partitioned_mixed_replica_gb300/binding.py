@@ -1,0 +1,250 @@
+"""ctypes binding of libzero (``include/zero.h``): same entry-point names,
+argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; nothing here computes.
+
+Device buffers are passed as torch tensors (their ``data_ptr()``) or raw
+integer addresses; pointer arrays as Python sequences of those.  Streams are
+``torch.cuda.Stream`` objects, raw handles, or ``None`` for torch's current
+stream.  A non-zero status raises :class:`ZeroError` with the library's
+message.  If ``libzero.so`` has not been built the first call raises — there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libzero.so")
+
+ZERO_OK = 0
+ZERO_ERR_INVALID = -1
+ZERO_ERR_ALIGN = -2
+ZERO_ERR_CUDA = -3
+ZERO_ERR_STATE = -4
+ZERO_ERR_TIMEOUT = -5
+ZERO_ERR_NOMEM = -6
+ZERO_BF16 = 0
+ZERO_FP16 = 1
+ZERO_MAX_RANKS = 64
+ZERO_OUT_FULL_REPLICAS = 0
+ZERO_OUT_SHARDS = 1
+ZERO_NORM_DECIDE = 0
+ZERO_NORM_AFTER_FUSED = 1
+
+EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero_layout_unit",
+            "zero_layout_tensor_offset", "zero_layout_destroy", "zero_state_init",
+            "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
+            "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
+            "zero_last_error", "zero_launch_count"]
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("libzero status %d: %s" % (status, msg))
+        self.status = status
+
+
+class zero_layout_info(ctypes.Structure):
+    _fields_ = ([(n, ctypes.c_int32) for n in ("n_d", "stage", "dtype", "n_tensors", "n_buckets",
+                                               "n_units", "reserved0", "reserved1")] +
+                [(n, ctypes.c_int64) for n in ("psi", "psi_pad", "q", "bucket_elems", "shard_len",
+                                               "max_unit_padded", "mem_formula", "mem_state",
+                                               "mem_gshard", "mem_transient", "mem_peak", "comm_rs",
+                                               "comm_ag", "comm_ag_fwd", "comm_ag_bwd",
+                                               "comm_allreduce", "comm_total", "workspace_bytes")])
+
+
+class zero_unit_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("offset", "real", "padded", "shard", "shard_base")]
+
+
+class zero_step_state(ctypes.Structure):
+    _fields_ = ([(n, ctypes.c_double) for n in ("beta1", "beta2", "beta1_pow", "beta2_pow", "grad_norm")] +
+                [("loss_scale", ctypes.c_float), ("clip_coef", ctypes.c_float)] +
+                [(n, ctypes.c_int32) for n in ("t", "skipped", "good_steps", "growth_interval",
+                                               "dynamic_scale", "nonfinite", "overflow", "apply",
+                                               "error")] +
+                [("reserved", ctypes.c_int32 * 3)])
+
+
+class zero_adamw_hp(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+assert ctypes.sizeof(zero_step_state) == 96
+
+_lib = None
+
+
+def lib():
+    """Load libzero.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libzero.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, dbl, flt = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_float
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "zero_layout_init": [ctypes.POINTER(i64), i32, ctypes.POINTER(i32), i32, i32, i64, i64, i32,
+                             ctypes.POINTER(P)],
+        "zero_layout_query": [P, ctypes.POINTER(zero_layout_info)],
+        "zero_layout_bucket": [P, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)],
+        "zero_layout_unit": [P, i32, ctypes.POINTER(zero_unit_info)],
+        "zero_layout_tensor_offset": [P, i32, ctypes.POINTER(i64)],
+        "zero_state_init": [P, dbl, dbl, flt, i32, i32, P],
+        "zero_reduce_scatter": [P, i32, PP, PP, P, P, P],
+        "zero_grad_norm": [P, dbl, i32, P, P, P],
+        "zero_adamw_shard_step": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
+        "zero_allgather_params": [P, PP, PP, P],
+        "zero_stage3_gather_layer": [P, i32, PP, PP, P],
+        "zero_fused_step": [P, i32, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = i32
+    L.zero_layout_destroy.argtypes = [P]
+    L.zero_layout_destroy.restype = None
+    L.zero_last_error.argtypes = []
+    L.zero_last_error.restype = ctypes.c_char_p
+    L.zero_launch_count.argtypes = [i32]
+    L.zero_launch_count.restype = i64
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != ZERO_OK:
+        raise ZeroError(status, lib().zero_last_error().decode())
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptrs(xs: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+class Layout:
+    """Owns a ``zero_layout*``; destroyed with the object."""
+
+    def __init__(self, handle: int):
+        self.handle = ctypes.c_void_p(handle)
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            _lib.zero_layout_destroy(h)
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+
+def zero_layout_init(numels: Sequence[int], unit_of_tensor: Optional[Sequence[int]], n_d: int, stage: int,
+                     pad_multiple: int = 0, bucket_elems: int = 0, dtype: int = ZERO_BF16) -> Layout:
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(n, 1))(*numels)
+    units = (ctypes.c_int32 * n)(*unit_of_tensor) if unit_of_tensor is not None else None
+    out = ctypes.c_void_p()
+    _check(lib().zero_layout_init(arr, n, units, n_d, stage, pad_multiple, bucket_elems, dtype,
+                                  ctypes.byref(out)))
+    return Layout(out.value)
+
+
+def zero_layout_query(L: Layout) -> zero_layout_info:
+    info = zero_layout_info()
+    _check(lib().zero_layout_query(L, ctypes.byref(info)))
+    return info
+
+
+def zero_layout_bucket(L: Layout, b: int):
+    b0, b1 = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zero_layout_bucket(L, b, ctypes.byref(b0), ctypes.byref(b1)))
+    return b0.value, b1.value
+
+
+def zero_layout_unit(L: Layout, u: int) -> zero_unit_info:
+    info = zero_unit_info()
+    _check(lib().zero_layout_unit(L, u, ctypes.byref(info)))
+    return info
+
+
+def zero_layout_tensor_offset(L: Layout, t: int) -> int:
+    off = ctypes.c_int64()
+    _check(lib().zero_layout_tensor_offset(L, t, ctypes.byref(off)))
+    return off.value
+
+
+def zero_layout_destroy(L: Layout) -> None:
+    h, L.handle = L.handle, None
+    if h:
+        lib().zero_layout_destroy(h)
+
+
+def zero_state_init(st, beta1: float, beta2: float, loss_scale: float = 1.0, dynamic_scale: bool = False,
+                    growth_interval: int = 2000, stream=None) -> None:
+    _check(lib().zero_state_init(_addr(st), beta1, beta2, loss_scale, int(dynamic_scale), growth_interval,
+                                 _stream(stream)))
+
+
+def zero_reduce_scatter(L: Layout, bucket_or_unit: int, grad_replicas, grad_shards, st, workspace,
+                        stream=None) -> None:
+    _check(lib().zero_reduce_scatter(L, bucket_or_unit, _ptrs(grad_replicas), _ptrs(grad_shards), _addr(st),
+                                     _addr(workspace), _stream(stream)))
+
+
+def zero_grad_norm(L: Layout, max_norm: float, flags: int, st, workspace, stream=None) -> None:
+    _check(lib().zero_grad_norm(L, max_norm, flags, _addr(st), _addr(workspace), _stream(stream)))
+
+
+def _hp(lr, eps, weight_decay) -> zero_adamw_hp:
+    return zero_adamw_hp(lr=lr, eps=eps, weight_decay=weight_decay)
+
+
+def zero_adamw_shard_step(L: Layout, hp: zero_adamw_hp, master, m, v, grad_shards, st, param16_out,
+                          out_kind: int, stream=None) -> None:
+    _check(lib().zero_adamw_shard_step(L, ctypes.byref(hp), _ptrs(master), _ptrs(m), _ptrs(v),
+                                       _ptrs(grad_shards), _addr(st), _ptrs(param16_out), out_kind,
+                                       _stream(stream)))
+
+
+def zero_allgather_params(L: Layout, param16_shards, param16_full, stream=None) -> None:
+    _check(lib().zero_allgather_params(L, _ptrs(param16_shards), _ptrs(param16_full), _stream(stream)))
+
+
+def zero_stage3_gather_layer(L: Layout, unit: int, param16_shards, transient, stream=None) -> None:
+    _check(lib().zero_stage3_gather_layer(L, unit, _ptrs(param16_shards), _ptrs(transient), _stream(stream)))
+
+
+def zero_fused_step(L: Layout, bucket_or_unit: int, hp: zero_adamw_hp, grad_replicas, master, m, v, st,
+                    param16_out, out_kind: int, workspace, stream=None) -> None:
+    _check(lib().zero_fused_step(L, bucket_or_unit, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master),
+                                 _ptrs(m), _ptrs(v), _addr(st), _ptrs(param16_out), out_kind,
+                                 _addr(workspace), _stream(stream)))
+
+
+def zero_last_error() -> str:
+    return lib().zero_last_error().decode()
+
+
+def zero_launch_count(reset: bool = False) -> int:
+    return int(lib().zero_launch_count(int(reset)))

@@ -1,0 +1,285 @@
+// Device-side building blocks of libzero (sm_103a).
+//
+// All floating-point arithmetic of the step goes through explicitly rounded
+// intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn, ...), so no
+// multiply-add is ever contracted and every operation is one IEEE-754
+// binary32 operation, round to nearest even.  The library is additionally
+// compiled with -fmad=false.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "zero.h"
+
+namespace zk {
+
+constexpr int kThreads = 256;      // threads per CTA of the streaming kernels
+constexpr int kVec = 8;            // 16-bit elements per 16-byte vector
+constexpr int kMaxRanks = ZERO_MAX_RANKS;
+
+// ----------------------------------------------------------------------------
+// 16-bit formats
+// ----------------------------------------------------------------------------
+struct Bf16 {
+    static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+    }
+    static __device__ __forceinline__ uint16_t enc1(float a) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    }
+    static __device__ __forceinline__ float dec1(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+};
+
+struct Fp16 {
+    static __device__ __forceinline__ float lo(uint32_t w) {
+        return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+    }
+    static __device__ __forceinline__ float hi(uint32_t w) {
+        return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    }
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        return (uint32_t)__half_as_ushort(__float2half_rn(a)) |
+               ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
+    }
+    static __device__ __forceinline__ uint16_t enc1(float a) { return __half_as_ushort(__float2half_rn(a)); }
+    static __device__ __forceinline__ float dec1(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+};
+
+template <class F>
+__device__ __forceinline__ void unpack8(const uint4& x, float (&o)[8]) {
+    o[0] = F::lo(x.x); o[1] = F::hi(x.x);
+    o[2] = F::lo(x.y); o[3] = F::hi(x.y);
+    o[4] = F::lo(x.z); o[5] = F::hi(x.z);
+    o[6] = F::lo(x.w); o[7] = F::hi(x.w);
+}
+
+template <class F>
+__device__ __forceinline__ uint4 pack8(const float (&p)[8]) {
+    uint4 r;
+    r.x = F::pack(p[0], p[1]);
+    r.y = F::pack(p[2], p[3]);
+    r.z = F::pack(p[4], p[5]);
+    r.w = F::pack(p[6], p[7]);
+    return r;
+}
+
+// ----------------------------------------------------------------------------
+// Memory access: every big buffer is streamed once per step.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ void st_stream(uint16_t* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+__device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+
+__device__ __forceinline__ void ld8(const float* p, float (&o)[8]) {
+    float4 a = ld_stream(p), b = ld_stream(p + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void st8(float* p, const float (&o)[8]) {
+    st_stream(p, make_float4(o[0], o[1], o[2], o[3]));
+    st_stream(p + 4, make_float4(o[4], o[5], o[6], o[7]));
+}
+
+// ----------------------------------------------------------------------------
+// Gradient reduction: s = x_0 + x_1 + ... in rank order; padding reads 0.
+// ND > 0: compile-time rank count; ND == 0: runtime `nd`.
+// ----------------------------------------------------------------------------
+template <int ND, class F>
+__device__ __forceinline__ void reduce8(const uint16_t* const* rep, int nd, uint32_t v,
+                                        int64_t real_end, float (&s)[8]) {
+    const int64_t i0 = (int64_t)v * kVec;
+    const int n = ND > 0 ? ND : nd;
+    if (i0 + kVec <= real_end) {
+        if constexpr (ND > 0) {
+            uint4 x[ND];
+#pragma unroll
+            for (int r = 0; r < ND; ++r) x[r] = ld_stream(rep[r] + i0);
+            unpack8<F>(x[0], s);
+#pragma unroll
+            for (int r = 1; r < ND; ++r) {
+                float t[8];
+                unpack8<F>(x[r], t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], t[e]);
+            }
+        } else {
+            uint4 x0 = ld_stream(rep[0] + i0);
+            unpack8<F>(x0, s);
+            int r = 1;
+            for (; r + 4 <= n; r += 4) {
+                uint4 x[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = ld_stream(rep[r + k] + i0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float t[8];
+                    unpack8<F>(x[k], t);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], t[e]);
+                }
+            }
+            for (; r < n; ++r) {
+                float t[8];
+                unpack8<F>(ld_stream(rep[r] + i0), t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = __fadd_rn(s[e], t[e]);
+            }
+        }
+    } else {
+        // Vector that reaches into (or lies in) the segment's padding: element
+        // loads, padding contributes exactly 0.
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[e] = 0.0f;
+        for (int e = 0; e < 8; ++e) {
+            if (i0 + e >= real_end) break;
+            float acc = F::dec1(rep[0][i0 + e]);
+            for (int r = 1; r < n; ++r) acc = __fadd_rn(acc, F::dec1(rep[r][i0 + e]));
+            s[e] = acc;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Sum of squares with an error-free transformation (Knuth's TwoSum and the
+// FMA-based TwoProduct; Ogita, Rump and Oishi, "Accurate Sum and Dot
+// Product", SIAM J. Sci. Comput. 26(6), 2005): (hi, lo) carries the running
+// sum and its accumulated rounding errors.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void acc_sq(float x, float& hi, float& lo) {
+    float p = __fmul_rn(x, x);
+    float pe = __fmaf_rn(x, x, -p);  // exact remainder x*x - p
+    float s, e;
+    two_sum(hi, p, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+
+// Combine with the partner lane `mask` away; symmetric, so both lanes end
+// with the same bits.
+__device__ __forceinline__ void combine_lanes(float& hi, float& lo, int mask) {
+    float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, mask);
+    float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, mask);
+    float s, e;
+    two_sum(hi, ohi, s, e);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, olo), e);
+}
+
+// 32-element group partial of 4 consecutive lanes (8 elements each).  All 32
+// lanes must call it.  Returns the group's sum of squares rounded once.
+__device__ __forceinline__ float group32_sumsq(const float (&g)[8]) {
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc_sq(g[e], hi, lo);
+    combine_lanes(hi, lo, 1);
+    combine_lanes(hi, lo, 2);
+    return __fadd_rn(hi, lo);
+}
+
+// ----------------------------------------------------------------------------
+// AdamW, decoupled weight decay, one rounding per operation.
+// ----------------------------------------------------------------------------
+struct AdamConsts {
+    float decay, b1, b2, omb1, omb2, eps, step_size, sqrt_bc2, clip;
+};
+
+// Constants of the step whose bias corrections are beta1^t = b1p and
+// beta2^t = b2p, computed in binary64 (IEEE division and square root) and
+// rounded once to binary32.
+__device__ __forceinline__ AdamConsts make_consts(double beta1, double beta2, double b1p, double b2p,
+                                                  double lr, double eps, double wd, float clip) {
+    AdamConsts k;
+    k.decay = __double2float_rn(__dsub_rn(1.0, __dmul_rn(lr, wd)));
+    k.b1 = __double2float_rn(beta1);
+    k.b2 = __double2float_rn(beta2);
+    k.omb1 = __double2float_rn(__dsub_rn(1.0, beta1));
+    k.omb2 = __double2float_rn(__dsub_rn(1.0, beta2));
+    k.eps = __double2float_rn(eps);
+    k.step_size = __double2float_rn(__ddiv_rn(lr, __dsub_rn(1.0, b1p)));
+    k.sqrt_bc2 = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, b2p)));
+    k.clip = clip;
+    return k;
+}
+
+__device__ __forceinline__ void adamw1(float& p, float& m, float& v, float g, const AdamConsts& k) {
+    const float gc = __fmul_rn(g, k.clip);
+    const float p1 = __fmul_rn(p, k.decay);
+    const float mn = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.omb1, gc));
+    const float vn = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.omb2, __fmul_rn(gc, gc)));
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(vn), k.sqrt_bc2), k.eps);
+    p = __fsub_rn(p1, __fmul_rn(k.step_size, __fdiv_rn(mn, den)));
+    m = mn;
+    v = vn;
+}
+
+// ----------------------------------------------------------------------------
+// Kernel arguments (passed by value as __grid_constant__ parameters).
+// Vector indices count 8-element vectors of the flat buffer (32-bit: the
+// layout rejects Psi_pad >= 2^35).
+// ----------------------------------------------------------------------------
+struct SegArgs {
+    uint32_t v_begin, v_end;  // flat vector range processed by this launch
+    uint32_t seg_v;           // segment offset (vectors)
+    uint32_t shard_v;         // S_u / 8
+    uint32_t base_v;          // shard_base / 8
+    uint32_t pad0;
+    int64_t real_end;         // flat index where the segment's padding starts
+};
+
+struct RsArgs {
+    const uint16_t* rep[kMaxRanks];
+    float* gshard[kMaxRanks];
+    float* partials;
+    zero_step_state* st;
+    SegArgs seg;
+    int32_t nd;
+};
+
+struct AdamArgs {
+    float* master[kMaxRanks];
+    float* m[kMaxRanks];
+    float* v[kMaxRanks];
+    const float* gshard[kMaxRanks];
+    uint16_t* out[kMaxRanks];
+    zero_step_state* st;
+    double lr, eps, wd;
+    uint32_t shard_v;   // per-rank shard length / 8
+    uint32_t total_v;   // nd * shard_v
+    int32_t nd;
+};
+
+struct FusedArgs {
+    const uint16_t* rep[kMaxRanks];
+    float* master[kMaxRanks];
+    float* m[kMaxRanks];
+    float* v[kMaxRanks];
+    uint16_t* out[kMaxRanks];
+    float* partials;
+    zero_step_state* st;
+    double lr, eps, wd;
+    SegArgs seg;
+    int32_t nd;
+};
+
+struct GatherArgs {
+    const uint16_t* src[kMaxRanks];
+    uint16_t* dst[kMaxRanks];
+    uint32_t shard_v;   // S_u / 8
+    uint32_t base_v;    // shard_base / 8
+    int64_t n_elems;    // elements per destination (real_u, or Psi_pad)
+    int32_t nd;
+};
+
+}  // namespace zk

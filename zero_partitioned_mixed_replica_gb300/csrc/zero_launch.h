@@ -1,0 +1,114 @@
+// Host-side launch helpers shared by libzero's CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+#include <string>
+
+#include "zero_device.cuh"
+#include "zero_internal.h"
+
+namespace zero_detail {
+
+inline int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Persistent grid: every CTA resident at once (SMs x resident CTAs per SM),
+// capped by the CTAs the work needs; kernels grid-stride over the rest.
+template <class Kernel>
+inline int persistent_grid(Kernel kernel, int64_t work_ctas) {
+    // resident CTAs per SM, cached per (device, kernel address)
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache[dev].find(reinterpret_cast<const void*>(kernel));
+        if (it != cache[dev].end()) per_sm = it->second;
+    }
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, zk::kThreads, 0) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev][reinterpret_cast<const void*>(kernel)] = per_sm;
+    }
+    int sms = sm_count();
+    if (sms <= 0) sms = 1;
+    int64_t cap = (int64_t)sms * per_sm;
+    int64_t g = work_ctas < cap ? work_ctas : cap;
+    return g < 1 ? 1 : (int)g;
+}
+
+inline zero_status_t check_dev_ptr(const void* p, const char* what) {
+    if (!p) return fail(ZERO_ERR_INVALID, std::string(what) + ": NULL device pointer");
+    if (reinterpret_cast<uintptr_t>(p) & 255u)
+        return fail(ZERO_ERR_ALIGN, std::string(what) + ": device pointer not 256-byte aligned");
+    return ZERO_OK;
+}
+
+inline zero_status_t check_ptr_array(const void* const* arr, int n, const char* what) {
+    if (!arr) return fail(ZERO_ERR_INVALID, std::string(what) + ": NULL pointer array");
+    for (int i = 0; i < n; ++i) {
+        zero_status_t s = check_dev_ptr(arr[i], what);
+        if (s != ZERO_OK) return s;
+    }
+    return ZERO_OK;
+}
+
+inline zero_status_t after_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(ZERO_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    count_launches(1);
+    return ZERO_OK;
+}
+
+inline zk::SegArgs seg_args(const zero_segment& s, int64_t begin, int64_t end) {
+    zk::SegArgs a;
+    a.v_begin = (uint32_t)(begin / zk::kVec);
+    a.v_end = (uint32_t)(end / zk::kVec);
+    a.seg_v = (uint32_t)(s.offset / zk::kVec);
+    a.shard_v = (uint32_t)(s.shard / zk::kVec);
+    a.base_v = (uint32_t)(s.shard_base / zk::kVec);
+    a.pad0 = 0;
+    a.real_end = s.offset + s.real;
+    return a;
+}
+
+}  // namespace zero_detail
+
+#define ZK_ND_SWITCH(nd, ...)                                  \
+    switch (nd) {                                              \
+        case 1: { constexpr int ND = 1; __VA_ARGS__; } break;  \
+        case 2: { constexpr int ND = 2; __VA_ARGS__; } break;  \
+        case 4: { constexpr int ND = 4; __VA_ARGS__; } break;  \
+        case 8: { constexpr int ND = 8; __VA_ARGS__; } break;  \
+        default: { constexpr int ND = 0; __VA_ARGS__; } break; \
+    }
+
+#define ZK_DISPATCH(nd, dtype, ...)                                  \
+    do {                                                             \
+        if ((dtype) == ZERO_BF16) {                                  \
+            using F = zk::Bf16;                                      \
+            ZK_ND_SWITCH(nd, __VA_ARGS__)                            \
+        } else {                                                     \
+            using F = zk::Fp16;                                      \
+            ZK_ND_SWITCH(nd, __VA_ARGS__)                            \
+        }                                                            \
+    } while (0)

@@ -1,0 +1,224 @@
+"""Step sequencer over the C ABI: one GPU, N_d simulated data-parallel ranks.
+
+:class:`ZeroStep` allocates every buffer once (torch is the allocator, in the
+spirit of the pre-allocated contiguous blocks of "ZeRO: Memory Optimizations
+Toward Training Trillion Parameter Models" reading notes §3.2.3/§5.3) and
+issues the library calls of one step in the order the pages give:
+
+* ZeRO-1/2, split (clipping or a loss scaler active): reduce-scatter bucket by
+  bucket, last bucket first (backward produces the last layers first; mlqm.cn
+  post "梯度桶化", reading notes §4.1-§4.2) -> global norm and step decision ->
+  sharded AdamW with the all-gather fused into its epilogue ("第 5 课：ZeRO 与
+  FSDP" §3).
+* ZeRO-1/2, fused (neither): reduce-scatter + AdamW + cast + all-gather in one
+  pass per bucket (or one pass for the whole buffer), then the norm report.
+* ZeRO-3: forward gathers unit by unit into the transient buffer; backward
+  walks the units in reverse, re-gathers each, reduce-scatters it and (fused)
+  updates its shard; no all-gather at the end of the step ("第 5 课" Fig. 5-1,
+  reading notes §3.1 and §4.3, "ZeRO-3 核心流程" §2).  With clipping or a scaler
+  the shard updates wait for the global decision.
+
+Every arithmetic step runs inside libzero's kernels; this module only owns
+memory, orders the calls and reads back the 96-byte step state.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import binding as B
+
+TORCH_16 = {B.ZERO_BF16: torch.bfloat16, B.ZERO_FP16: torch.float16}
+
+
+@dataclass
+class AdamW:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+
+
+class ZeroStep:
+    def __init__(self, numels: Sequence[int], n_d: int, stage: int, dtype: int = B.ZERO_BF16,
+                 bucket_elems: int = 0, unit_of_tensor: Optional[Sequence[int]] = None,
+                 adamw: AdamW = AdamW(), max_norm: float = 0.0, loss_scale: float = 1.0,
+                 dynamic_scale: bool = False, growth_interval: int = 2000,
+                 fused: Optional[bool] = None, per_bucket: bool = True, fuse_allgather: bool = True,
+                 device: str = "cuda", stream: Optional[torch.cuda.Stream] = None):
+        if stage not in (1, 2, 3):
+            raise ValueError("ZeroStep runs ZeRO stages 1, 2 and 3")
+        self.L = B.zero_layout_init(list(numels), list(unit_of_tensor) if unit_of_tensor is not None else None,
+                                    n_d, stage, 0, bucket_elems, dtype)
+        self.info = B.zero_layout_query(self.L)
+        self.n_d, self.stage, self.dtype = n_d, stage, dtype
+        self.adamw = adamw
+        self.max_norm = float(max_norm)
+        self.loss_scale0 = float(loss_scale)
+        self.dynamic, self.growth_interval = bool(dynamic_scale), int(growth_interval)
+        no_scaler = (not dynamic_scale) and loss_scale == 1.0
+        self.fused = (self.max_norm <= 0 and no_scaler) if fused is None else bool(fused)
+        if self.fused and not (self.max_norm <= 0 and no_scaler):
+            raise ValueError("the fused step cannot clip or skip: use the split step")
+        self.per_bucket = per_bucket
+        # ZeRO-1/2 split step only: False writes 16-bit shards, then all-gathers them
+        self.fuse_allgather = fuse_allgather or stage == 3 or self.fused
+        self.device = torch.device(device)
+        self.stream = stream
+        dt16 = TORCH_16[dtype]
+        P, S = self.info.psi_pad, self.info.shard_len
+        dev = self.device
+        self.n_buckets = self.info.n_buckets
+        self.units = [B.zero_layout_unit(self.L, u) for u in range(self.info.n_units)]
+        self.tensor_offsets = [B.zero_layout_tensor_offset(self.L, t) for t in range(len(numels))]
+        self.numels = list(numels)
+        # rank-major 2-D allocations; row r is rank r's buffer (rows stay 256-byte aligned)
+        self.grads = torch.zeros(n_d, P, dtype=dt16, device=dev)
+        self.master = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
+        self.m = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
+        self.gshard = None if self.fused else torch.zeros(n_d, S, dtype=torch.float32, device=dev)
+        if stage == 3:
+            self.params = None
+            self.shard16 = torch.zeros(n_d, S, dtype=dt16, device=dev)
+            max_real = max(u.real for u in self.units)
+            self.transient = torch.zeros(n_d, (max_real + 127) // 128 * 128, dtype=dt16, device=dev)
+        else:
+            self.params = torch.zeros(n_d, P, dtype=dt16, device=dev)
+            self.shard16 = None if self.fuse_allgather else torch.zeros(n_d, S, dtype=dt16, device=dev)
+            self.transient = None
+        self.workspace = torch.zeros(self.info.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.state = torch.zeros(96, dtype=torch.uint8, device=dev)
+        self._rows()
+        self.hp = B.zero_adamw_hp(lr=adamw.lr, eps=adamw.eps, weight_decay=adamw.weight_decay)
+        self.transient_hook = None  # called as hook(kind, unit, transient_rows) after each ZeRO-3 gather
+        self.reset_state()
+
+    # -- pointer lists ---------------------------------------------------------
+    def _rows(self):
+        rows = lambda t: [t[r] for r in range(self.n_d)] if t is not None else None
+        self.grad_rows = rows(self.grads)
+        self.master_rows, self.m_rows, self.v_rows = rows(self.master), rows(self.m), rows(self.v)
+        self.gshard_rows = rows(self.gshard)
+        self.param_rows = rows(self.params)
+        self.shard16_rows = rows(self.shard16)
+        self.transient_rows = rows(self.transient)
+
+    def _s(self):
+        return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
+
+    # -- initialisation (plumbing, not part of the step) -------------------------
+    def reset_state(self):
+        B.zero_state_init(self.state, self.adamw.beta1, self.adamw.beta2, self.loss_scale0, self.dynamic,
+                          self.growth_interval, self._s())
+
+    def load_master(self, flat_master: torch.Tensor) -> None:
+        """Scatter a flat fp32 master (Psi_pad, zero padding) into the rank
+        shards, zero m and v, and set the 16-bit parameters to its
+        round-to-nearest-even cast."""
+        assert flat_master.numel() == self.info.psi_pad
+        fm = flat_master.to(self.device, torch.float32)
+        for u in self.units:
+            for r in range(self.n_d):
+                lo = u.offset + r * u.shard
+                self.master[r, u.shard_base:u.shard_base + u.shard].copy_(fm[lo:lo + u.shard])
+        self.m.zero_()
+        self.v.zero_()
+        p16 = fm.to(TORCH_16[self.dtype])
+        if self.shard16 is not None:
+            for u in self.units:
+                for r in range(self.n_d):
+                    lo = u.offset + r * u.shard
+                    self.shard16[r, u.shard_base:u.shard_base + u.shard].copy_(p16[lo:lo + u.shard])
+        if self.params is not None:
+            self.params.copy_(p16.unsqueeze(0).expand(self.n_d, -1))
+
+    # -- the step ------------------------------------------------------------------
+    def step(self) -> None:
+        s = self._s()
+        L, nd = self.L, self.n_d
+        if self.stage == 3:
+            U = len(self.units)
+            for u in range(U):                                   # forward
+                B.zero_stage3_gather_layer(L, u, self.shard16_rows, self.transient_rows, s)
+                if self.transient_hook:
+                    self.transient_hook("fwd", u, self.transient_rows)
+            for u in reversed(range(U)):                         # backward
+                B.zero_stage3_gather_layer(L, u, self.shard16_rows, self.transient_rows, s)
+                if self.transient_hook:
+                    self.transient_hook("bwd", u, self.transient_rows)
+                if self.fused:
+                    B.zero_fused_step(L, u, self.hp, self.grad_rows, self.master_rows, self.m_rows,
+                                      self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
+                                      self.workspace, s)
+                else:
+                    B.zero_reduce_scatter(L, u, self.grad_rows, self.gshard_rows, self.state, self.workspace, s)
+            if self.fused:
+                B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
+            else:
+                B.zero_grad_norm(L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
+                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows,
+                                        self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
+            return
+        if self.fused:
+            if self.per_bucket:
+                for b in reversed(range(self.n_buckets)):
+                    B.zero_fused_step(L, b, self.hp, self.grad_rows, self.master_rows, self.m_rows,
+                                      self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
+                                      self.workspace, s)
+            else:
+                B.zero_fused_step(L, -1, self.hp, self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
+                                  self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, self.workspace, s)
+            B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
+        else:
+            for b in reversed(range(self.n_buckets)):
+                B.zero_reduce_scatter(L, b, self.grad_rows, self.gshard_rows, self.state, self.workspace, s)
+            B.zero_grad_norm(L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
+            if self.fuse_allgather:
+                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows, self.gshard_rows,
+                                        self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, s)
+            else:
+                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows, self.gshard_rows,
+                                        self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
+                B.zero_allgather_params(L, self.shard16_rows, self.param_rows, s)
+
+    # -- CUDA graph of one step -------------------------------------------------------
+    def capture(self) -> torch.cuda.CUDAGraph:
+        """Record one step into a CUDA graph (the step allocates nothing and
+        never synchronises, so it captures as is).  Replaying the graph runs
+        one step."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        old = self.stream
+        with torch.cuda.stream(side):
+            self.stream = side
+            with torch.cuda.graph(g, stream=side):
+                self.step()
+        self.stream = old
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        return g
+
+    # -- readback -------------------------------------------------------------------
+    def read_state(self) -> dict:
+        torch.cuda.synchronize(self.device)
+        raw = bytes(self.state.cpu().numpy().tobytes())
+        st = B.zero_step_state.from_buffer_copy(raw)
+        return {"t": st.t, "skipped": st.skipped, "overflow": st.overflow, "apply": st.apply,
+                "grad_norm": st.grad_norm, "clip_coef": st.clip_coef, "loss_scale": st.loss_scale,
+                "good_steps": st.good_steps, "nonfinite": st.nonfinite, "error": st.error,
+                "beta1_pow": st.beta1_pow, "beta2_pow": st.beta2_pow}
+
+    def flat(self, which: str) -> torch.Tensor:
+        """Reassemble master/m/v (fp32) or shard16 (ZeRO-3) into flat order."""
+        src = {"master": self.master, "m": self.m, "v": self.v, "shard16": self.shard16,
+               "gshard": self.gshard}[which]
+        out = torch.zeros(self.info.psi_pad, dtype=src.dtype, device=src.device)
+        for u in self.units:
+            for r in range(self.n_d):
+                lo = u.offset + r * u.shard
+                out[lo:lo + u.shard].copy_(src[r, u.shard_base:u.shard_base + u.shard])
+        return out
