@@ -1,0 +1,382 @@
+#!/usr/bin/env python
+"""Benchmark of the ZeRO-DP partitioned mixed-precision AdamW step on GB300.
+
+Metric: ZeRO step params/s (and achieved HBM GB/s, % of 8 TB/s) for the GPT-2
+1.5B layout (48 blocks, d = 1600, ffn 6400, vocab 50257, tied head; Psi =
+1,557,611,200) with N_d = 8 simulated ranks, ZeRO-2, fp16 gradients under a
+dynamic loss scale of 2^16 and global-norm clipping at 1.0.  One step = the
+whole hot path over one batch of synthetic gradients resident in HBM:
+4 bucketed reduce-scatters (bucket 5e8, last first) -> two-pass global norm and
+step decision -> sharded AdamW with the all-gather fused in.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gpt2_xl|gpt2_small|llama7b|tiny]
+
+Under torchrun (N > 1) every rank runs its own independent replica of the
+step on its own GPU (the simulated ranks live inside one GPU; there is no
+data-path collective); a gloo barrier brackets the timed region and rank 0
+prints the max-over-ranks time.  ``--impl reference`` times the CPU oracle on
+the host cores instead (rank 0 only), on a bounded sample of the same
+workload.  One JSON line is printed by rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO step params/s and achieved HBM GB/s (% of 8 TB/s) at Ψ=1.5B, N_d=8"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["zero_rs.cu", "zero_adamw.cu", "zero_norm.cu", "zero_gather.cu", "zero_device.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="gpt2_xl")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size in parameters")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload arithmetic
+# ---------------------------------------------------------------------------
+
+def bytes_per_param(w, fused: bool) -> float:
+    """Algorithmic HBM bytes per parameter per step (16-bit = 2 bytes)."""
+    nd = w.n_d
+    if w.stage == 3:
+        if fused:
+            return 2 * (2 + 2 * nd) + 2 * nd + 24 + 2        # 2 gathers + RS + AdamW + shard write
+        return 2 * (2 + 2 * nd) + 2 * nd + 4 + 4 + 24 + 2
+    if fused:
+        return 4 * nd + 24
+    return 4 * nd + 24 + min(2 * nd, 8)
+
+
+def kernel_bytes(name: str, w, elems: int) -> float:
+    nd = w.n_d
+    per = {"reduce_scatter": 2 * nd + 4, "adamw": 4 + 24 + (2 * nd if w.stage != 3 else 2),
+           "fused_step": 2 * nd + 24 + (2 * nd if w.stage != 3 else 2), "stage3_gather": 2 + 2 * nd,
+           "allgather": 2 + 2 * nd, "grad_norm": 4 / 32}[name]
+    return per * elems
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "zero_partitioned_mixed_replica_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, if
+    it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out = ""
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_timing(w, sample_params: int, min_seconds: float, min_steps: int = 3, max_steps: int = 10 ** 6):
+    import numpy as np
+    from oracle.layout import make_layout
+    from oracle.step import AdamWHP, ZeroSimulation, num_threads
+    from zero_partitioned_mixed_replica_gb300 import synth
+
+    numels = [sample_params]
+    units = [0] if w.stage == 3 else None
+    L = make_layout(numels, w.n_d, w.stage, bucket_elems=w.bucket_elems if w.stage != 3 else 0,
+                    unit_of_tensor=units)
+    m0 = synth.master_init(numels, L.tensor_offsets, L.psi_pad, w.master_std).numpy()
+    reps = [synth.as_u16(synth.grad_replica(numels, L.tensor_offsets, L.psi_pad, w.dtype, r, 1, w.grad_std,
+                                            None, w.loss_scale)) for r in range(w.n_d)]
+    zs = ZeroSimulation(L, m0, w.dtype, AdamWHP(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay),
+                        max_norm=w.max_norm, loss_scale=w.loss_scale, dynamic=w.dynamic_scale,
+                        growth_interval=w.growth_interval)
+    zs.step(reps)                                   # warm-up
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps and (n < min_steps or time.perf_counter() - t0 < min_seconds):
+        zs.step(reps)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": sample_params / dt, "unit": "params/s", "cores": num_threads(), "kind": "oracle",
+            "sample": "%d parameters (%.3f%% of the workload), N_d=%d, stage %d, %d timed steps of %.3f s"
+                      % (sample_params, 100.0 * sample_params / w.psi, w.n_d, w.stage, n, dt),
+            "s_per_step": dt, "steps": n}
+
+
+def default_sample(w) -> int:
+    return min(w.psi, max(1 << 20, 16_000_000 if w.n_d <= 8 else 4_000_000))
+
+
+# ---------------------------------------------------------------------------
+# GPU run
+# ---------------------------------------------------------------------------
+
+def gpu_run(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from zero_partitioned_mixed_replica_gb300 import binding as B
+    from zero_partitioned_mixed_replica_gb300 import build as zbuild
+    from zero_partitioned_mixed_replica_gb300 import synth
+    from zero_partitioned_mixed_replica_gb300.engine import AdamW, ZeroStep
+
+    zbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    units = w.unit_of_tensor if w.stage == 3 else None
+    eng = ZeroStep(w.numels, w.n_d, w.stage, w.dtype, w.bucket_elems if w.stage != 3 else 0, units,
+                   AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay), w.max_norm, w.loss_scale,
+                   w.dynamic_scale, w.growth_interval, device=str(dev))
+    info = eng.info
+    m0 = synth.master_init(w.numels, eng.tensor_offsets, info.psi_pad, w.master_std, device=dev)
+    eng.load_master(m0)
+    del m0
+    scales = synth.tensor_scales(len(w.numels)) if w.per_tensor_scale else None
+    for r in range(w.n_d):
+        synth.grad_replica(w.numels, eng.tensor_offsets, info.psi_pad, w.dtype, r, 1, w.grad_std, scales,
+                           w.loss_scale, device=dev, out=eng.grads[r])
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    graph = eng.capture() if args.graph else None
+    run = (lambda: graph.replay()) if graph is not None else eng.step
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize(dev)
+    # --- timed region -----------------------------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)
+    if graph is None:
+        eng.timers = {}
+    B.zero_launch_count(reset=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = B.zero_launch_count()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    timers, eng.timers = eng.timers, None
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if graph is not None:
+        # launches inside a replayed graph are the captured ones
+        B.zero_launch_count(reset=True)
+        eng.step()
+        torch.cuda.synchronize(dev)
+        launches = B.zero_launch_count() * args.steps
+    st = eng.read_state()
+
+    # --- per-kernel averages from events on the launching stream ------------------
+    kern = {}
+    if timers:
+        for name, evs in timers.items():
+            d = [a.elapsed_time(b) for a, b in evs]
+            kern[name] = {"launches": len(d), "total_ms": sum(d), "avg_ms": sum(d) / len(d)}
+    # --- e2e: host buffers, H2D of the step's gradients + D2H of the step result ----
+    e2e = None
+    if args.e2e_steps > 0:
+        try:
+            host_grads = torch.empty(tuple(eng.grads.shape), dtype=eng.grads.dtype, pin_memory=True)
+            host_grads.copy_(eng.grads)
+            host_state = torch.empty(96, dtype=torch.uint8).pin_memory()
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.e2e_steps):
+                eng.grads.copy_(host_grads, non_blocking=True)
+                eng.step()
+                host_state.copy_(eng.state, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ems = a.elapsed_time(b)
+            if world > 1:
+                t = torch.tensor([ems], dtype=torch.float64)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                ems = float(t.item())
+            e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
+                   "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()),
+                   "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps}
+            del host_grads
+        except RuntimeError as ex:
+            e2e = {"value": None, "unit": "params/s", "error": str(ex)[:200]}
+    return eng, info, ms, kern, launches, clk, st, e2e
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from zero_partitioned_mixed_replica_gb300 import workloads
+    w = workloads.ALL[args.workload]()
+    fused = w.fused()
+    bpp = bytes_per_param(w, fused)
+    workload_desc = {"workload": w.name, "psi": w.psi, "n_d": w.n_d, "stage": w.stage,
+                     "grad_dtype": "fp16" if w.dtype == 1 else "bf16", "state_dtype": "fp32",
+                     "bucket_elems": w.bucket_elems, "max_norm": w.max_norm, "loss_scale": w.loss_scale,
+                     "algorithmic_bytes_per_param": bpp,
+                     "l2": "no flush: the step streams > 60 GB per pass, far above the 129 MB L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample = args.cpu_sample or default_sample(w)
+        cb = oracle_timing(w, sample, min_seconds=max(1.0, args.cpu_seconds), min_steps=max(1, args.steps))
+        line = {"metric": METRIC, "value": cb["value"], "unit": "params/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": cb["steps"], "warmup": 1,
+                "ms_per_step": cb["s_per_step"] * 1e3 * w.psi / sample,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "config": workload_desc,
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": cb["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    eng, info, ms, kern, launches, clk, st, e2e = gpu_run(args, w, rank, world, local_rank)
+    step_s = ms / 1e3 / args.steps
+    value = world * w.psi / step_s
+    step_gbs = bpp * info.psi_pad / step_s / 1e9
+    peak, peak_kind = measured_peak()
+    roof = None
+    if kern:
+        dom = max(kern, key=lambda k: kern[k]["total_ms"])
+        if dom in ("reduce_scatter", "fused_step"):
+            elems = info.psi_pad / max(1, kern[dom]["launches"] // args.steps)
+        elif dom == "stage3_gather":
+            elems = 2 * w.psi / max(1, kern[dom]["launches"] // args.steps)
+        else:
+            elems = info.psi_pad
+        ach = kernel_bytes(dom, w, elems) / (kern[dom]["avg_ms"] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "peak_kind": peak_kind + " (copy bandwidth)",
+                "traffic": ncu_traffic(dom, args.workload),
+                "algorithmic_bytes_per_launch": kernel_bytes(dom, w, elems),
+                "avg_launch_ms": kern[dom]["avg_ms"]}
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        sample = args.cpu_sample or default_sample(w)
+        cb = oracle_timing(w, sample, min_seconds=args.cpu_seconds)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_desc,
+            "hbm_gbs": step_gbs, "hbm_pct_of_8tbs": 100.0 * step_gbs / NOMINAL_HBM_GBS,
+            "hbm_frac_of_measured_copy": step_gbs / peak,
+            "gpu_launches": launches, "clocks": clk, "e2e": e2e, "roofline": roof, "cpu_baseline": cpu,
+            "kernels": kern, "graph": bool(args.graph),
+            "last_step_state": {k: st[k] for k in ("t", "skipped", "overflow", "grad_norm", "clip_coef",
+                                                   "loss_scale")}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -95,6 +95,7 @@ class ZeroStep:
         self._rows()
         self.hp = B.zero_adamw_hp(lr=adamw.lr, eps=adamw.eps, weight_decay=adamw.weight_decay)
         self.transient_hook = None  # called as hook(kind, unit, transient_rows) after each ZeRO-3 gather
+        self.timers = None          # dict: call name -> list of (start, end) CUDA events, when timing
         self.reset_state()
 
     # -- pointer lists ---------------------------------------------------------
@@ -109,6 +110,19 @@ class ZeroStep:
 
     def _s(self):
         return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
+
+    def _call(self, name: str, fn, *args):
+        """Issue one library call; with ``timers`` set, bracket it by CUDA
+        events recorded on the launching stream."""
+        if self.timers is None:
+            fn(*args)
+            return
+        s = self._s()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn(*args)
+        b.record(s)
+        self.timers.setdefault(name, []).append((a, b))
 
     # -- initialisation (plumbing, not part of the step) -------------------------
     def reset_state(self):
@@ -139,51 +153,55 @@ class ZeroStep:
     # -- the step ------------------------------------------------------------------
     def step(self) -> None:
         s = self._s()
-        L, nd = self.L, self.n_d
+        L, C = self.L, self._call
         if self.stage == 3:
             U = len(self.units)
             for u in range(U):                                   # forward
-                B.zero_stage3_gather_layer(L, u, self.shard16_rows, self.transient_rows, s)
+                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
                 if self.transient_hook:
                     self.transient_hook("fwd", u, self.transient_rows)
             for u in reversed(range(U)):                         # backward
-                B.zero_stage3_gather_layer(L, u, self.shard16_rows, self.transient_rows, s)
+                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
                 if self.transient_hook:
                     self.transient_hook("bwd", u, self.transient_rows)
                 if self.fused:
-                    B.zero_fused_step(L, u, self.hp, self.grad_rows, self.master_rows, self.m_rows,
-                                      self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
-                                      self.workspace, s)
+                    C("fused_step", B.zero_fused_step, L, u, self.hp, self.grad_rows, self.master_rows,
+                      self.m_rows, self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
+                      self.workspace, s)
                 else:
-                    B.zero_reduce_scatter(L, u, self.grad_rows, self.gshard_rows, self.state, self.workspace, s)
+                    C("reduce_scatter", B.zero_reduce_scatter, L, u, self.grad_rows, self.gshard_rows,
+                      self.state, self.workspace, s)
             if self.fused:
-                B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
+                C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
             else:
-                B.zero_grad_norm(L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
-                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows,
-                                        self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
+                C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state,
+                  self.workspace, s)
+                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
+                  self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
             return
         if self.fused:
             if self.per_bucket:
                 for b in reversed(range(self.n_buckets)):
-                    B.zero_fused_step(L, b, self.hp, self.grad_rows, self.master_rows, self.m_rows,
-                                      self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
-                                      self.workspace, s)
+                    C("fused_step", B.zero_fused_step, L, b, self.hp, self.grad_rows, self.master_rows,
+                      self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
+                      self.workspace, s)
             else:
-                B.zero_fused_step(L, -1, self.hp, self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
-                                  self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, self.workspace, s)
-            B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
+                C("fused_step", B.zero_fused_step, L, -1, self.hp, self.grad_rows, self.master_rows,
+                  self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
+                  self.workspace, s)
+            C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
         else:
             for b in reversed(range(self.n_buckets)):
-                B.zero_reduce_scatter(L, b, self.grad_rows, self.gshard_rows, self.state, self.workspace, s)
-            B.zero_grad_norm(L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
+                C("reduce_scatter", B.zero_reduce_scatter, L, b, self.grad_rows, self.gshard_rows, self.state,
+                  self.workspace, s)
+            C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
             if self.fuse_allgather:
-                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows, self.gshard_rows,
-                                        self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, s)
+                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
+                  self.gshard_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, s)
             else:
-                B.zero_adamw_shard_step(L, self.hp, self.master_rows, self.m_rows, self.v_rows, self.gshard_rows,
-                                        self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
-                B.zero_allgather_params(L, self.shard16_rows, self.param_rows, s)
+                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
+                  self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
+                C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
 
     # -- CUDA graph of one step -------------------------------------------------------
     def capture(self) -> torch.cuda.CUDAGraph:

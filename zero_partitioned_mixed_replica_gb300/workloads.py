@@ -115,6 +115,18 @@ def gpt2_xl() -> Workload:
                     loss_scale=65536.0, dynamic_scale=True, steps=10, inf_step=4, inf_rank=3)
 
 
+def gpt2_xl_block() -> Workload:
+    """One GPT-2 1.5B transformer block (30.7M parameters) with the 1.5B
+    run's settings: the same kernels on a buffer small enough (~1.5 GB on the
+    device, still far above L2) for multi-pass profiler captures."""
+    numels, units = gpt2_tensors(1, 1600, 6400)
+    numels, units = numels[2:-2], [0] * (len(numels) - 4)
+    return Workload("one GPT-2 1.5B block (30.7M), N_d=8, ZeRO-2, fp16, loss scale 2^16, clip 1.0",
+                    numels, units, n_d=8, stage=2, dtype=FP16, bucket_elems=500_000_000,
+                    grad_std=1e-3, per_tensor_scale=True, max_norm=1.0,
+                    loss_scale=65536.0, dynamic_scale=True, steps=10)
+
+
 def llama7b() -> Workload:
     numels, units = llama_tensors()
     return Workload("Llama-style 7B, N_d=2, ZeRO-3 (33 units), bf16",
@@ -133,4 +145,5 @@ def gpt2_medium_odd(n_d: int = 8, stage: int = 2, bucket_elems: int = 5_000_000)
 
 
 ALL = {"tiny": tiny, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl, "llama7b": llama7b,
+       "gpt2_xl_block": gpt2_xl_block,
        "gpt2_medium": gpt2_medium_odd}
