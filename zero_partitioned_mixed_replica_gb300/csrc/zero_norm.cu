@@ -39,17 +39,25 @@ __global__ void state_init_kernel(zero_step_state* st, double beta1, double beta
     st->reserved[0] = st->reserved[1] = st->reserved[2] = 0;
 }
 
-// Pass 1: block b sums a fixed contiguous range of the partials in binary64
-// (fixed thread-strided assignment, then a fixed pairwise tree).
+// Pass 1: block b sums a fixed contiguous range of the partials (fixed
+// thread-strided assignment).  Each thread accumulates in binary32 with an
+// error-free TwoSum carry (hi + lo holds the sum to ~2^-48 relative; binary64
+// arithmetic is slow on this part), then the block combines the threads'
+// hi + lo in binary64 through a fixed pairwise tree.
 __global__ void __launch_bounds__(256) norm_blocks_kernel(const float* __restrict__ partials, uint32_t count,
                                                           double* __restrict__ block_sums) {
     const uint32_t chunk = (count + gridDim.x - 1) / gridDim.x;
     const uint32_t b0 = blockIdx.x * chunk;
     const uint32_t b1 = min(count, b0 + chunk);
-    double s = 0.0;
-    for (uint32_t i = b0 + threadIdx.x; i < b1; i += blockDim.x) s = __dadd_rn(s, (double)partials[i]);
+    float hi = 0.0f, lo = 0.0f;
+    for (uint32_t i = b0 + threadIdx.x; i < b1; i += blockDim.x) {
+        float s, e;
+        two_sum(hi, partials[i], s, e);
+        hi = s;
+        lo = __fadd_rn(lo, e);
+    }
     __shared__ double sh[256];
-    sh[threadIdx.x] = s;
+    sh[threadIdx.x] = __dadd_rn((double)hi, (double)lo);
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
         if ((int)threadIdx.x < w) sh[threadIdx.x] = __dadd_rn(sh[threadIdx.x], sh[threadIdx.x + w]);
