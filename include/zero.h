@@ -291,6 +291,40 @@ zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
                               zero_step_state* st, void* const* param16_out, int32_t out_kind,
                               void* workspace, zero_stream_t stream);
 
+/* Largest Psi_pad that zero_fused_step_noalloc accepts (64 Mi elements). */
+#define ZERO_NOALLOC_MAX_ELEMS 67108864
+
+/* zero_fused_step over the whole buffer (every bucket; for ZeRO-3 every unit,
+ * last unit first), followed by zero_grad_norm(..., ZERO_NORM_AFTER_FUSED),
+ * for callers that cannot provide a device workspace.  The pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * Who needs it: code that may not allocate device memory when it runs, for
+ * example a plug-in inside a host application that owns all device memory
+ * through its own pool, or a latency-critical loop where a cudaMalloc (which
+ * can synchronise the device) is not allowed.  Instead of a caller workspace,
+ * the norm scratch lives in a fixed array compiled into the library: 8 MiB +
+ * 8 KiB of device memory that every GPU loading the library keeps until the
+ * process exits.  The call itself allocates nothing.
+ *
+ * Limits and behaviour:
+ *   - Psi_pad must not exceed ZERO_NOALLOC_MAX_ELEMS, else ZERO_ERR_INVALID
+ *     (nothing is launched).  Stage 0: ZERO_ERR_STATE.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture begins.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing needs clearing, because each call writes every slot before it
+ *     reads it.  Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array: serialise them.
+ *   - Arguments, outputs and the update are those of zero_fused_step (no
+ *     clipping, no loss-scale skip); ZeRO-3 requires ZERO_OUT_SHARDS. */
+zero_status_t zero_fused_step_noalloc(const zero_layout* L, const zero_adamw_hp* hp,
+                                      const void* const* grad_replicas, float* const* master,
+                                      float* const* m, float* const* v, zero_step_state* st,
+                                      void* const* param16_out, int32_t out_kind,
+                                      zero_stream_t stream);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* zero_last_error(void);
 

@@ -37,7 +37,8 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_layout_tensor_offset", "zero_layout_destroy", "zero_state_init",
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
             "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
-            "zero_last_error", "zero_launch_count"]
+            "zero_fused_step_noalloc", "zero_last_error", "zero_launch_count"]
+ZERO_NOALLOC_MAX_ELEMS = 67108864
 
 
 class ZeroError(RuntimeError):
@@ -102,6 +103,7 @@ def lib():
         "zero_allgather_params": [P, PP, PP, P],
         "zero_stage3_gather_layer": [P, i32, PP, PP, P],
         "zero_fused_step": [P, i32, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P, P],
+        "zero_fused_step_noalloc": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -240,6 +242,13 @@ def zero_fused_step(L: Layout, bucket_or_unit: int, hp: zero_adamw_hp, grad_repl
     _check(lib().zero_fused_step(L, bucket_or_unit, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master),
                                  _ptrs(m), _ptrs(v), _addr(st), _ptrs(param16_out), out_kind,
                                  _addr(workspace), _stream(stream)))
+
+
+def zero_fused_step_noalloc(L: Layout, hp: zero_adamw_hp, grad_replicas, master, m, v, st, param16_out,
+                            out_kind: int, stream=None) -> None:
+    """Whole fused step without a caller workspace (see include/zero.h)."""
+    _check(lib().zero_fused_step_noalloc(L, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master), _ptrs(m),
+                                         _ptrs(v), _addr(st), _ptrs(param16_out), out_kind, _stream(stream)))
 
 
 def zero_last_error() -> str:
