@@ -110,6 +110,18 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time (gloo all-reduce MAX on the host); the value
+    itself on a single rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -253,10 +265,7 @@ def gpu_run(args, w, rank, world, local_rank):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     timers, eng.timers = eng.timers, None
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     if graph is not None:
         # launches inside a replayed graph are the captured ones
         B.zero_launch_count(reset=True)
@@ -289,11 +298,7 @@ def gpu_run(args, w, rank, world, local_rank):
                 host_state.copy_(eng.state, non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize(dev)
-            ems = a.elapsed_time(b)
-            if world > 1:
-                t = torch.tensor([ems], dtype=torch.float64)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                ems = float(t.item())
+            ems = max_over_ranks(a.elapsed_time(b), world)
             e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
                    "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()),
                    "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps}
