@@ -51,6 +51,11 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    p.add_argument("--whole-buffer", action="store_true",
+                   help="fused path: one launch over the whole buffer instead of one per bucket")
+    p.add_argument("--sweep", action="store_true",
+                   help="350M+1 layout: GB/s vs bucket size and N_d for stages 1/2/3 (one JSON line per point)")
+    p.add_argument("--sweep-nd", default="2,4,8,16,64")
     return p.parse_args()
 
 
@@ -224,7 +229,7 @@ def gpu_run(args, w, rank, world, local_rank):
     units = w.unit_of_tensor if w.stage == 3 else None
     eng = ZeroStep(w.numels, w.n_d, w.stage, w.dtype, w.bucket_elems if w.stage != 3 else 0, units,
                    AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay), w.max_norm, w.loss_scale,
-                   w.dynamic_scale, w.growth_interval, device=str(dev))
+                   w.dynamic_scale, w.growth_interval, per_bucket=not args.whole_buffer, device=str(dev))
     info = eng.info
     m0 = synth.master_init(w.numels, eng.tensor_offsets, info.psi_pad, w.master_std, device=dev)
     eng.load_master(m0)
@@ -308,8 +313,60 @@ def gpu_run(args, w, rank, world, local_rank):
     return eng, info, ms, kern, launches, clk, st, e2e
 
 
+def sweep(args):
+    """GB/s vs bucket size and N_d on the GPT-2 medium 350M + 1 layout (odd
+    Psi), fused step (no clipping, no scaler), stages 1/2 per bucket and
+    stage 3 per unit.  Rank 0's gradients are drawn by the input generator and
+    copied to the other ranks (values do not change the traffic)."""
+    import torch
+    from zero_partitioned_mixed_replica_gb300 import binding as B
+    from zero_partitioned_mixed_replica_gb300 import build as zbuild
+    from zero_partitioned_mixed_replica_gb300 import synth, workloads
+    from zero_partitioned_mixed_replica_gb300.engine import ZeroStep
+    zbuild.build()
+    dev = torch.device("cuda", 0)
+    buckets = [100_000, 500_000, 1_000_000, 5_000_000, 10_000_000, 50_000_000]
+    for nd in [int(x) for x in args.sweep_nd.split(",")]:
+        for stage in (1, 2, 3):
+            w = workloads.gpt2_medium_odd(n_d=nd, stage=stage, bucket_elems=buckets[0])
+            eng = ZeroStep(w.numels, nd, stage, w.dtype, buckets[0] if stage != 3 else 0,
+                           w.unit_of_tensor if stage == 3 else None, device=str(dev))
+            eng.load_master(synth.master_init(w.numels, eng.tensor_offsets, eng.info.psi_pad, device=dev))
+            synth.grad_replica(w.numels, eng.tensor_offsets, eng.info.psi_pad, w.dtype, 0, 1, w.grad_std,
+                               synth.tensor_scales(len(w.numels)), device=dev, out=eng.grads[0])
+            for r in range(1, nd):
+                eng.grads[r].copy_(eng.grads[0])
+            bpp = bytes_per_param(w, True)
+            for b in (buckets if stage != 3 else [0]):
+                if stage != 3:
+                    eng.set_bucket_elems(b)
+                for _ in range(2):
+                    eng.step()
+                torch.cuda.synchronize(dev)
+                B.zero_launch_count(reset=True)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    eng.step()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                ms = e0.elapsed_time(e1) / args.steps
+                print(json.dumps({"sweep": "gpt2_medium_350M+1", "n_d": nd, "stage": stage,
+                                  "bucket_elems": b if stage != 3 else "per unit",
+                                  "n_buckets": eng.n_buckets if stage != 3 else len(eng.units),
+                                  "ms_per_step": ms, "params_per_s": w.psi / (ms / 1e3),
+                                  "hbm_gbs": bpp * eng.info.psi_pad / (ms / 1e3) / 1e9,
+                                  "bytes_per_param": bpp,
+                                  "launches_per_step": B.zero_launch_count() // args.steps}), flush=True)
+            del eng
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.sweep:
+        sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

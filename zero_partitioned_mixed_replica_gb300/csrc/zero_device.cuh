@@ -76,14 +76,17 @@ __device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(rein
 __device__ __forceinline__ void st_stream(uint16_t* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
 __device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+// 8 consecutive floats as one 32-byte access (sm_100+ 256-bit vector form),
+// cache-streaming; p must be 32-byte aligned.
 __device__ __forceinline__ void ld8(const float* p, float (&o)[8]) {
-    float4 a = ld_stream(p), b = ld_stream(p + 4);
-    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
-    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    asm volatile("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]), "=f"(o[7])
+                 : "l"(p));
 }
 __device__ __forceinline__ void st8(float* p, const float (&o)[8]) {
-    st_stream(p, make_float4(o[0], o[1], o[2], o[3]));
-    st_stream(p + 4, make_float4(o[4], o[5], o[6], o[7]));
+    asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(o[0]), "f"(o[1]), "f"(o[2]),
+                 "f"(o[3]), "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7])
+                 : "memory");
 }
 
 // ----------------------------------------------------------------------------

@@ -14,7 +14,7 @@
 namespace zk {
 
 template <int ND, class F>
-__global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ RsArgs a) {
+__device__ __forceinline__ void rs_body(const RsArgs& a) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
     const uint32_t nw = (gridDim.x * kThreads) >> 5;
@@ -46,16 +46,24 @@ __global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ Rs
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0u) atomicOr(&a.st->nonfinite, 1);
 }
 
+template <int ND, class F>
+__global__ void __launch_bounds__(kThreads) rs_kernel(const __grid_constant__ RsArgs a) {
+    rs_body<ND, F>(a);
+}
+
 }  // namespace zk
 
 using namespace zero_detail;
 
+template <class K>
+static zero_status_t launch_rs_kernel(K kern, const zk::RsArgs& a, int64_t nvec, cudaStream_t s) {
+    kern<<<persistent_grid(kern, (nvec + zk::kThreads - 1) / zk::kThreads), zk::kThreads, 0, s>>>(a);
+    return after_launch("zero_reduce_scatter");
+}
+
 template <int ND, class F>
 static zero_status_t launch_rs(const zk::RsArgs& a, int64_t nvec, cudaStream_t s) {
-    auto kern = zk::rs_kernel<ND, F>;
-    const int grid = persistent_grid(kern, (nvec + zk::kThreads - 1) / zk::kThreads);
-    kern<<<grid, zk::kThreads, 0, s>>>(a);
-    return after_launch("zero_reduce_scatter");
+    return launch_rs_kernel(zk::rs_kernel<ND, F>, a, nvec, s);
 }
 
 extern "C" zero_status_t zero_reduce_scatter(const zero_layout* L, int32_t bucket_or_unit,
@@ -87,6 +95,7 @@ extern "C" zero_status_t zero_reduce_scatter(const zero_layout* L, int32_t bucke
     const int64_t nvec = (bk.second - bk.first) / zk::kVec;
     if (nvec == 0) return ZERO_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    ZK_DISPATCH(L->n_d, L->dtype, return launch_rs<ND, F>(a, nvec, s));
+    const int nd = L->n_d;
+    ZK_DISPATCH(nd, L->dtype, return launch_rs<ND, F>(a, nvec, s));
     return ZERO_OK;
 }

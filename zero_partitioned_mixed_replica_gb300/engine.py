@@ -98,6 +98,16 @@ class ZeroStep:
         self.timers = None          # dict: call name -> list of (start, end) CUDA events, when timing
         self.reset_state()
 
+    def set_bucket_elems(self, bucket_elems: int) -> None:
+        """Re-lay the same buffers with another bucket size (ZeRO-1/2): the
+        padded length and shards do not depend on it, so nothing moves."""
+        if self.stage == 3:
+            raise ValueError("ZeRO-3 reduces per unit")
+        L = B.zero_layout_init(self.numels, None, self.n_d, self.stage, 0, bucket_elems, self.dtype)
+        info = B.zero_layout_query(L)
+        assert info.psi_pad == self.info.psi_pad and info.shard_len == self.info.shard_len
+        self.L, self.info, self.n_buckets = L, info, info.n_buckets
+
     # -- pointer lists ---------------------------------------------------------
     def _rows(self):
         rows = lambda t: [t[r] for r in range(self.n_d)] if t is not None else None
