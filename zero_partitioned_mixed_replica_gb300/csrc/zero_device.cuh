@@ -89,6 +89,52 @@ __device__ __forceinline__ void st8(float* p, const float (&o)[8]) {
                  : "memory");
 }
 
+// 16 consecutive 16-bit values as one 32-byte access; p 32-byte aligned.
+__device__ __forceinline__ void ld16h(const uint16_t* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+template <class F>
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float (&o)[16]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        o[2 * k] = F::lo(w[k]);
+        o[2 * k + 1] = F::hi(w[k]);
+    }
+}
+
+// 16-element form of reduce8 (compile-time ND only): all N_d loads are issued
+// before the rank-order sum.
+template <int ND, class F>
+__device__ __forceinline__ void reduce16(const uint16_t* const* rep, uint32_t v16, int64_t real_end,
+                                         float (&s)[16]) {
+    const int64_t i0 = (int64_t)v16 * 16;
+    if (i0 + 16 <= real_end) {
+        uint32_t w[ND][8];
+#pragma unroll
+        for (int r = 0; r < ND; ++r) ld16h(rep[r] + i0, w[r]);
+        unpack16<F>(w[0], s);
+#pragma unroll
+        for (int r = 1; r < ND; ++r) {
+            float t[16];
+            unpack16<F>(w[r], t);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s[e] = __fadd_rn(s[e], t[e]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) s[e] = 0.0f;
+        for (int e = 0; e < 16; ++e) {
+            if (i0 + e >= real_end) break;
+            float acc = F::dec1(rep[0][i0 + e]);
+            for (int r = 1; r < ND; ++r) acc = __fadd_rn(acc, F::dec1(rep[r][i0 + e]));
+            s[e] = acc;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------
 // Gradient reduction: s = x_0 + x_1 + ... in rank order; padding reads 0.
 // ND > 0: compile-time rank count; ND == 0: runtime `nd`.
