@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="350M+1 layout: GB/s vs bucket size and N_d for stages 1/2/3 (one JSON line per point)")
     p.add_argument("--sweep-nd", default="2,4,8,16,64")
+    p.add_argument("--checkpoint", default="",
+                   help="directory: time a sharded checkpoint save and a load resharded to N_d/2 (one JSON line)")
     return p.parse_args()
 
 
@@ -362,10 +364,46 @@ def sweep(args):
             torch.cuda.empty_cache()
 
 
+def checkpoint_bench(args):
+    """Sharded checkpoint of the chosen workload: every simulated rank writes
+    its shard in parallel; then a layout with half the ranks (ZeRO-2) loads it
+    through the reshard plan."""
+    import shutil
+    import torch
+    from zero_partitioned_mixed_replica_gb300 import build as zbuild
+    from zero_partitioned_mixed_replica_gb300 import synth, workloads
+    from zero_partitioned_mixed_replica_gb300.engine import ZeroStep
+    zbuild.build()
+    w = workloads.ALL[args.workload]()
+    units = w.unit_of_tensor if w.stage == 3 else None
+    a = ZeroStep(w.numels, w.n_d, w.stage, w.dtype, w.bucket_elems if w.stage != 3 else 0, units)
+    a.load_master(synth.master_init(w.numels, a.tensor_offsets, a.info.psi_pad, device=a.device))
+    path = os.path.join(args.checkpoint, "ckpt")
+    shutil.rmtree(path, ignore_errors=True)
+    t0 = time.perf_counter()
+    out = a.save_checkpoint(path)
+    t_save = time.perf_counter() - t0
+    nd2 = max(1, w.n_d // 2)
+    del a
+    torch.cuda.empty_cache()
+    b = ZeroStep(w.numels, nd2, 2, w.dtype, w.bucket_elems if w.bucket_elems > 0 else 0, None)
+    t0 = time.perf_counter()
+    info = b.load_checkpoint(path)
+    t_load = time.perf_counter() - t0
+    shutil.rmtree(path, ignore_errors=True)
+    print(json.dumps({"checkpoint": w.name, "bytes": out["bytes"], "save_s": t_save, "load_s": t_load,
+                      "save_gbs": out["bytes"] / t_save / 1e9, "load_gbs": info["bytes"] / t_load / 1e9,
+                      "reshard": "N_d %d stage %d -> N_d %d stage 2" % (w.n_d, w.stage, nd2),
+                      "segments": info["segments"]}), flush=True)
+
+
 def main():
     args = parse()
     if args.sweep:
         sweep(args)
+        return
+    if args.checkpoint:
+        checkpoint_bench(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

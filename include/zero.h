@@ -187,6 +187,27 @@ zero_status_t zero_layout_unit(const zero_layout* L, int32_t u, zero_unit_info* 
 zero_status_t zero_layout_tensor_offset(const zero_layout* L, int32_t t, int64_t* offset);
 void zero_layout_destroy(zero_layout* L);
 
+/* One contiguous copy of the reshard plan: len elements from rank src_rank's
+ * shard at src_off to rank dst_rank's shard at dst_off. */
+typedef struct zero_copy_segment {
+    int32_t src_rank, dst_rank;
+    int64_t src_off, dst_off, len;
+} zero_copy_segment;
+
+/* Resharding plan between two layouts of the same tensors (sharded
+ * checkpoints: each rank saves its own shard, "別再複製本可分片的東西：ZeRO 與
+ * FSDP", 分片檢查點; loading into another N_d, stage or unit split needs every
+ * real element's new home).  Host only, integer work.  Every real element of
+ * every tensor appears in exactly one segment; padding in neither.  Segments
+ * are maximal (contiguous in both shard spaces), in src flat order.
+ *   src, dst   layouts with equal tensor counts and sizes (any n_d, stage 1-3).
+ *   out        capacity segments, or NULL to query the count.
+ *   *count     number of segments the plan needs.
+ * Returns ZERO_ERR_INVALID if the tensors differ, a layout is stage 0, or
+ * capacity is too small (with *count set). */
+zero_status_t zero_reshard_plan(const zero_layout* src, const zero_layout* dst, zero_copy_segment* out,
+                                int64_t capacity, int64_t* count);
+
 /* ------------------------------------------------------------------------ */
 /* Step state                                                                */
 /* ------------------------------------------------------------------------ */

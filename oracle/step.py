@@ -289,6 +289,29 @@ class ZeroSimulation:
         self.transients: List[Tuple[str, int, List[np.ndarray]]] = []
         self.record_transients = False
 
+    @classmethod
+    def from_flat(cls, L: Layout, master: np.ndarray, m: np.ndarray, v: np.ndarray, fmt: int, hp: AdamWHP,
+                  state: StepState, max_norm: float = 0.0) -> "ZeroSimulation":
+        """A simulation of layout L whose optimizer state is the given flat
+        master/m/v (Psi_pad of L, zero padding) — what loading a sharded
+        checkpoint into another layout must reach."""
+        zs = cls(L, master, fmt, hp, max_norm=max_norm, loss_scale=state.loss_scale, dynamic=state.dynamic,
+                 growth_interval=state.growth_interval)
+        for name, flat in (("m", m), ("v", v)):
+            dst = getattr(zs, name)
+            for r in range(L.n_d):
+                for u in L.units:
+                    lo = u.offset + r * u.shard
+                    dst[r][u.shard_base:u.shard_base + u.shard] = flat[lo:lo + u.shard]
+        zs.state = StepState(state.loss_scale, state.dynamic, state.growth_interval, state.t, state.skipped,
+                             state.good)
+        return zs
+
+    def flat_real(self, which: str) -> np.ndarray:
+        """Concatenation of every tensor's values (no padding), in tensor order."""
+        flat = self.flat(which)
+        return np.concatenate([flat[o:o + n] for o, n in zip(self.L.tensor_offsets, self.L.numels)])
+
     # -- collectives ---------------------------------------------------------
     def _allgather(self, p16_shards: List[np.ndarray]) -> None:
         """All-gather (ZeRO-1/2): every rank's full replica receives every

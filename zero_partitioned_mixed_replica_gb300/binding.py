@@ -37,7 +37,7 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_layout_tensor_offset", "zero_layout_destroy", "zero_state_init",
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
             "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
-            "zero_fused_step_noalloc", "zero_last_error", "zero_launch_count"]
+            "zero_fused_step_noalloc", "zero_reshard_plan", "zero_last_error", "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
 
@@ -68,6 +68,11 @@ class zero_step_state(ctypes.Structure):
                                                "dynamic_scale", "nonfinite", "overflow", "apply",
                                                "error")] +
                 [("reserved", ctypes.c_int32 * 3)])
+
+
+class zero_copy_segment(ctypes.Structure):
+    _fields_ = [("src_rank", ctypes.c_int32), ("dst_rank", ctypes.c_int32), ("src_off", ctypes.c_int64),
+                ("dst_off", ctypes.c_int64), ("len", ctypes.c_int64)]
 
 
 class zero_adamw_hp(ctypes.Structure):
@@ -104,6 +109,7 @@ def lib():
         "zero_stage3_gather_layer": [P, i32, PP, PP, P],
         "zero_fused_step": [P, i32, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P, P],
         "zero_fused_step_noalloc": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
+        "zero_reshard_plan": [P, P, ctypes.POINTER(zero_copy_segment), i64, ctypes.POINTER(i64)],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -249,6 +255,15 @@ def zero_fused_step_noalloc(L: Layout, hp: zero_adamw_hp, grad_replicas, master,
     """Whole fused step without a caller workspace (see include/zero.h)."""
     _check(lib().zero_fused_step_noalloc(L, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master), _ptrs(m),
                                          _ptrs(v), _addr(st), _ptrs(param16_out), out_kind, _stream(stream)))
+
+
+def zero_reshard_plan(src: Layout, dst: Layout):
+    """List of (src_rank, src_off, dst_rank, dst_off, len) copy segments."""
+    n = ctypes.c_int64()
+    _check(lib().zero_reshard_plan(src, dst, None, 0, ctypes.byref(n)))
+    arr = (zero_copy_segment * max(1, n.value))()
+    _check(lib().zero_reshard_plan(src, dst, arr, n.value, ctypes.byref(n)))
+    return [(g.src_rank, g.src_off, g.dst_rank, g.dst_off, g.len) for g in arr[:n.value]]
 
 
 def zero_last_error() -> str:

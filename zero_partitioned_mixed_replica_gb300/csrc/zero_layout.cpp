@@ -240,3 +240,62 @@ extern "C" zero_status_t zero_layout_tensor_offset(const zero_layout* L, int32_t
 }
 
 extern "C" void zero_layout_destroy(zero_layout* L) { delete L; }
+
+// Where flat index i lives: (rank, shard offset, elements left in that shard).
+static void locate(const zero_layout* L, int64_t i, int32_t* rank, int64_t* off, int64_t* left) {
+    size_t lo = 0, hi = L->segs.size();
+    while (hi - lo > 1) {  // last segment with offset <= i
+        size_t mid = (lo + hi) / 2;
+        if (L->segs[mid].offset <= i) lo = mid; else hi = mid;
+    }
+    const zero_segment& s = L->segs[lo];
+    const int64_t k = i - s.offset;
+    const int64_t r = k / s.shard;
+    *rank = (int32_t)r;
+    *off = s.shard_base + (k - r * s.shard);
+    *left = s.shard - (k - r * s.shard);
+}
+
+extern "C" zero_status_t zero_reshard_plan(const zero_layout* src, const zero_layout* dst,
+                                           zero_copy_segment* out, int64_t capacity, int64_t* count) {
+    clear_error();
+    if (!src || !dst || !count) return fail(ZERO_ERR_INVALID, "reshard: null argument");
+    if (src->stage == 0 || dst->stage == 0) return fail(ZERO_ERR_INVALID, "reshard: stage 0 has no shards");
+    if (src->numels != dst->numels) return fail(ZERO_ERR_INVALID, "reshard: layouts hold different tensors");
+    int64_t n = 0;
+    bool have = false;
+    zero_copy_segment cur{};
+    auto emit = [&](const zero_copy_segment& g) {
+        if (have && cur.src_rank == g.src_rank && cur.dst_rank == g.dst_rank &&
+            cur.src_off + cur.len == g.src_off && cur.dst_off + cur.len == g.dst_off) {
+            cur.len += g.len;
+            return;
+        }
+        if (have) {
+            if (out && n < capacity) out[n] = cur;
+            ++n;
+        }
+        cur = g;
+        have = true;
+    };
+    for (size_t t = 0; t < src->numels.size(); ++t) {
+        const int64_t total = src->numels[t];
+        int64_t pos = 0;
+        while (pos < total) {
+            zero_copy_segment g{};
+            int64_t ls, ld;
+            locate(src, src->tensor_offset[t] + pos, &g.src_rank, &g.src_off, &ls);
+            locate(dst, dst->tensor_offset[t] + pos, &g.dst_rank, &g.dst_off, &ld);
+            g.len = std::min(std::min(ls, ld), total - pos);
+            emit(g);
+            pos += g.len;
+        }
+    }
+    if (have) {
+        if (out && n < capacity) out[n] = cur;
+        ++n;
+    }
+    *count = n;
+    if (out && n > capacity) return fail(ZERO_ERR_INVALID, "reshard: capacity too small");
+    return ZERO_OK;
+}

@@ -23,9 +23,13 @@ memory, orders the calls and reads back the 96-byte step state.
 """
 from __future__ import annotations
 
+import json
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
+import numpy as np
 import torch
 
 from . import binding as B
@@ -75,6 +79,7 @@ class ZeroStep:
         self.units = [B.zero_layout_unit(self.L, u) for u in range(self.info.n_units)]
         self.tensor_offsets = [B.zero_layout_tensor_offset(self.L, t) for t in range(len(numels))]
         self.numels = list(numels)
+        self.unit_of_tensor = list(unit_of_tensor) if unit_of_tensor is not None else None
         # rank-major 2-D allocations; row r is rank r's buffer (rows stay 256-byte aligned)
         self.grads = torch.zeros(n_d, P, dtype=dt16, device=dev)
         self.master = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
@@ -229,6 +234,93 @@ class ZeroStep:
         self.stream = old
         torch.cuda.current_stream(self.device).wait_stream(side)
         return g
+
+    # -- sharded checkpoints ("別再複製本可分片的東西：ZeRO 與 FSDP": each rank dumps
+    #    its own shard in parallel) ---------------------------------------------------
+    def _shard16_rows_view(self):
+        if self.shard16 is not None:
+            return [self.shard16[r] for r in range(self.n_d)]
+        S = self.info.shard_len     # ZeRO-1/2 fused all-gather: rank r's slice of its replica
+        return [self.params[r, r * S:(r + 1) * S] for r in range(self.n_d)]
+
+    def save_checkpoint(self, path: str) -> dict:
+        """Write one file per simulated rank (its fp32 master/m/v shard and
+        16-bit parameter shard), in parallel, plus meta.json with the layout
+        and the 96-byte step state.  Returns the bytes written."""
+        os.makedirs(path, exist_ok=True)
+        torch.cuda.synchronize(self.device)
+        p16 = self._shard16_rows_view()
+
+        def dump(r):
+            with open(os.path.join(path, "rank%03d.bin" % r), "wb") as f:
+                for t in (self.master[r], self.m[r], self.v[r]):
+                    f.write(t.cpu().numpy().tobytes())
+                f.write(p16[r].contiguous().view(torch.int16).cpu().numpy().tobytes())
+            return 14 * self.info.shard_len
+
+        with ThreadPoolExecutor(max_workers=min(16, self.n_d)) as ex:
+            nbytes = sum(ex.map(dump, range(self.n_d)))
+        meta = {"format": "zero-shard-v1", "numels": self.numels,
+                "unit_of_tensor": self.unit_of_tensor, "n_d": self.n_d, "stage": self.stage,
+                "dtype": self.dtype, "bucket_elems": int(self.info.bucket_elems),
+                "psi_pad": int(self.info.psi_pad), "shard_len": int(self.info.shard_len),
+                "state": bytes(self.state.cpu().numpy().tobytes()).hex()}
+        with open(os.path.join(path, "meta.json"), "w") as f:
+            json.dump(meta, f)
+        return {"bytes": nbytes}
+
+    def load_checkpoint(self, path: str) -> dict:
+        """Load a checkpoint written by any layout of the same tensors (other
+        N_d, stage or unit split): the library's reshard plan maps every real
+        element to its shard here; each of this layout's ranks is assembled on
+        the host and uploaded once per array.  The 16-bit replicas of ZeRO-1/2
+        are rebuilt from the shards by the all-gather kernel."""
+        with open(os.path.join(path, "meta.json")) as f:
+            meta = json.load(f)
+        if meta.get("format") != "zero-shard-v1":
+            raise ValueError("not a zero-shard-v1 checkpoint")
+        src = B.zero_layout_init(meta["numels"], meta["unit_of_tensor"] if meta["stage"] == 3 else None,
+                                 meta["n_d"], meta["stage"], 0, meta["bucket_elems"], meta["dtype"])
+        if meta["dtype"] != self.dtype:
+            raise ValueError("checkpoint dtype differs")
+        plan = B.zero_reshard_plan(src, self.L)
+        S0, S = meta["shard_len"], self.info.shard_len
+        files = [np.memmap(os.path.join(path, "rank%03d.bin" % r), dtype=np.uint8, mode="r")
+                 for r in range(meta["n_d"])]
+        views = []
+        for mm in files:
+            f32 = mm[:12 * S0].view(np.float32)
+            views.append((f32[:S0], f32[S0:2 * S0], f32[2 * S0:3 * S0], mm[12 * S0:14 * S0].view(np.uint16)))
+        by_dst = {r: [] for r in range(self.n_d)}
+        for seg in plan:
+            by_dst[seg[2]].append(seg)
+        p16_rows = self._shard16_rows_view()
+
+        def assemble(r):
+            host = [np.zeros(S, np.float32) for _ in range(3)] + [np.zeros(S, np.uint16)]
+            for sr, so, dr, do, n in by_dst[r]:
+                for k in range(4):
+                    host[k][do:do + n] = views[sr][k][so:so + n]
+            return r, host
+
+        with ThreadPoolExecutor(max_workers=min(16, self.n_d)) as ex:
+            for r, host in ex.map(assemble, range(self.n_d)):
+                self.master[r].copy_(torch.from_numpy(host[0]))
+                self.m[r].copy_(torch.from_numpy(host[1]))
+                self.v[r].copy_(torch.from_numpy(host[2]))
+                p16_rows[r].view(torch.int16).copy_(torch.from_numpy(host[3].view(np.int16)))
+        st = bytes.fromhex(meta["state"])
+        self.state.copy_(torch.frombuffer(bytearray(st), dtype=torch.uint8))
+        if self.stage != 3:
+            if self.shard16 is None:
+                shards = torch.stack([t.clone() for t in p16_rows])
+                B.zero_allgather_params(self.L, [shards[r] for r in range(self.n_d)], self.param_rows, self._s())
+                torch.cuda.synchronize(self.device)
+                del shards
+            else:
+                B.zero_allgather_params(self.L, self.shard16_rows, self.param_rows, self._s())
+        torch.cuda.synchronize(self.device)
+        return {"segments": len(plan), "bytes": 14 * S * self.n_d}
 
     # -- readback -------------------------------------------------------------------
     def read_state(self) -> dict:
