@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = "ZeRO step params/s and achieved HBM GB/s (% of 8 TB/s) at Ψ=1.5B, N_d=8"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["zero_rs.cu", "zero_adamw.cu", "zero_norm.cu", "zero_gather.cu", "zero_device.cuh"]
+KERNEL_SOURCES = ["zero_rs.cu", "zero_adamw.cu", "zero_norm.cu", "zero_gather.cu", "zero_device.cuh",
+                  "zero_accum.cu"]
 
 
 def parse():
@@ -56,6 +57,8 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="350M+1 layout: GB/s vs bucket size and N_d for stages 1/2/3 (one JSON line per point)")
     p.add_argument("--sweep-nd", default="2,4,8,16,64")
+    p.add_argument("--micro", type=int, default=1,
+                   help="micro-batches per optimizer step (gradient accumulation, split step)")
     p.add_argument("--checkpoint", default="",
                    help="directory: time a sharded checkpoint save and a load resharded to N_d/2 (one JSON line)")
     return p.parse_args()
@@ -65,9 +68,22 @@ def parse():
 # workload arithmetic
 # ---------------------------------------------------------------------------
 
-def bytes_per_param(w, fused: bool) -> float:
-    """Algorithmic HBM bytes per parameter per step (16-bit = 2 bytes)."""
+def bytes_per_param(w, fused: bool, n_micro: int = 1) -> float:
+    """Algorithmic HBM bytes per parameter per optimizer step (16-bit = 2
+    bytes).  With n_micro > 1 micro-batches (split step): ZeRO-1 accumulates
+    each rank's full gradient in fp32 (first 6 N_d, then 10 N_d per micro-batch)
+    and reduce-scatters the accumulators once (4 N_d + 4); ZeRO-2/3 reduce every
+    micro-batch into the fp32 shard (2 N_d + 4 first, 2 N_d + 8 after); ZeRO-3
+    gathers forward and backward every micro-batch."""
     nd = w.n_d
+    M = n_micro
+    if M > 1:
+        adamw = 28 + (2 if w.stage == 3 else 2 * nd)
+        if w.stage == 1:
+            return 6 * nd + 10 * nd * (M - 1) + 4 * nd + 4 + adamw
+        rs = 2 * nd * M + 4 + 8 * (M - 1)
+        gathers = 2 * (2 + 2 * nd) * M if w.stage == 3 else 0
+        return rs + gathers + adamw
     if w.stage == 3:
         if fused:
             return 2 * (2 + 2 * nd) + 2 * nd + 24 + 2        # 2 gathers + RS + AdamW + shard write
@@ -79,7 +95,8 @@ def bytes_per_param(w, fused: bool) -> float:
 
 def kernel_bytes(name: str, w, elems: int) -> float:
     nd = w.n_d
-    per = {"reduce_scatter": 2 * nd + 4, "adamw": 4 + 24 + (2 * nd if w.stage != 3 else 2),
+    per = {"reduce_scatter": 2 * nd + 4, "accumulate": 10 * nd,
+           "adamw": 4 + 24 + (2 * nd if w.stage != 3 else 2),
            "fused_step": 2 * nd + 24 + (2 * nd if w.stage != 3 else 2), "stage3_gather": 2 + 2 * nd,
            "allgather": 2 + 2 * nd, "grad_norm": 4 / 32}[name]
     return per * elems
@@ -231,7 +248,8 @@ def gpu_run(args, w, rank, world, local_rank):
     units = w.unit_of_tensor if w.stage == 3 else None
     eng = ZeroStep(w.numels, w.n_d, w.stage, w.dtype, w.bucket_elems if w.stage != 3 else 0, units,
                    AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay), w.max_norm, w.loss_scale,
-                   w.dynamic_scale, w.growth_interval, per_bucket=not args.whole_buffer, device=str(dev))
+                   w.dynamic_scale, w.growth_interval, per_bucket=not args.whole_buffer, n_micro=args.micro,
+                   device=str(dev))
     info = eng.info
     m0 = synth.master_init(w.numels, eng.tensor_offsets, info.psi_pad, w.master_std, device=dev)
     eng.load_master(m0)
@@ -243,7 +261,12 @@ def gpu_run(args, w, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     graph = eng.capture() if args.graph else None
-    run = (lambda: graph.replay()) if graph is not None else eng.step
+    if args.micro > 1:
+        def run():
+            for mb in range(args.micro):
+                eng.micro_step(mb)
+    else:
+        run = (lambda: graph.replay()) if graph is not None else eng.step
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize(dev)
@@ -300,14 +323,15 @@ def gpu_run(args, w, rank, world, local_rank):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(args.e2e_steps):
-                eng.grads.copy_(host_grads, non_blocking=True)
-                eng.step()
+                for mb in range(args.micro):
+                    eng.grads.copy_(host_grads, non_blocking=True)
+                    eng.micro_step(mb)
                 host_state.copy_(eng.state, non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize(dev)
             ems = max_over_ranks(a.elapsed_time(b), world)
             e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
-                   "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()),
+                   "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()) * args.micro,
                    "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps}
             del host_grads
         except RuntimeError as ex:
@@ -410,12 +434,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     from zero_partitioned_mixed_replica_gb300 import workloads
     w = workloads.ALL[args.workload]()
-    fused = w.fused()
-    bpp = bytes_per_param(w, fused)
+    fused = w.fused() and args.micro == 1
+    bpp = bytes_per_param(w, fused, args.micro)
     workload_desc = {"workload": w.name, "psi": w.psi, "n_d": w.n_d, "stage": w.stage,
                      "grad_dtype": "fp16" if w.dtype == 1 else "bf16", "state_dtype": "fp32",
                      "bucket_elems": w.bucket_elems, "max_norm": w.max_norm, "loss_scale": w.loss_scale,
-                     "algorithmic_bytes_per_param": bpp,
+                     "algorithmic_bytes_per_param": bpp, "micro_batches": args.micro,
                      "l2": "no flush: the step streams > 60 GB per pass, far above the 129 MB L2"}
 
     if args.impl == "reference":
@@ -446,7 +470,9 @@ def main():
     roof = None
     if kern:
         dom = max(kern, key=lambda k: kern[k]["total_ms"])
-        if dom in ("reduce_scatter", "fused_step"):
+        if dom == "accumulate":
+            elems = info.psi_pad
+        elif dom in ("reduce_scatter", "fused_step"):
             elems = info.psi_pad / max(1, kern[dom]["launches"] // args.steps)
         elif dom == "stage3_gather":
             elems = 2 * w.psi / max(1, kern[dom]["launches"] // args.steps)

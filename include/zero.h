@@ -312,6 +312,45 @@ zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
                               zero_step_state* st, void* const* param16_out, int32_t out_kind,
                               void* workspace, zero_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Gradient accumulation over M micro-batches per optimizer step             */
+/* ------------------------------------------------------------------------ */
+/* Reading notes "ZeRO: Memory Optimizations ..." §4.1: with P_os (ZeRO-1)
+ * gradient accumulation needs no extra communication — every rank keeps its
+ * full gradient and accumulates locally; §4.2 (ZeRO-2) and §4.3 (ZeRO-3)
+ * reduce-scatter every micro-batch.  "第 5 课：ZeRO 与 FSDP" §2: fp32
+ * accumulation costs 4 Psi per rank for ZeRO-1 and 4 Psi / N_d for ZeRO-2/3.
+ * The averaged gradient is g = (sum over micro-batches and ranks) /
+ * (N_d * M * loss_scale); the two schedules sum in different orders:
+ *   ZeRO-1:   A_r = x_{r,0} + x_{r,1} + ...  then  g = (A_0 + A_1 + ...) / D
+ *   ZeRO-2/3: acc = s_0 + s_1 + ...  (s_m: rank-order sum of micro-batch m),
+ *             then g = acc / D. */
+
+/* ZeRO-1 local accumulation of micro-batch `micro` (0-based): for every rank
+ * r and flat index i, acc_replicas[r][i] = x (micro 0) or acc + x (binary32),
+ * x = grad_replicas[r][i] (padding reads 0).  acc_replicas: N_d fp32 buffers
+ * of Psi_pad elements.  Stage 1 only (ZERO_ERR_STATE otherwise). */
+zero_status_t zero_accumulate_grads(const zero_layout* L, int32_t micro, const void* const* grad_replicas,
+                                    float* const* acc_replicas, zero_stream_t stream);
+
+/* ZeRO-1 reduce-scatter of the fp32 accumulators of one bucket after the
+ * last micro-batch: s = A_0 + A_1 + ... in rank order, grad_shards[r][j] =
+ * s / (N_d * n_micro * loss_scale), plus norm partials and the non-finite
+ * flag (as zero_reduce_scatter).  Stage 1 only. */
+zero_status_t zero_reduce_scatter_accumulated(const zero_layout* L, int32_t bucket, const float* const* acc_replicas,
+                                              float* const* grad_shards, int32_t n_micro, zero_step_state* st,
+                                              void* workspace, zero_stream_t stream);
+
+/* ZeRO-2/3 reduce-scatter of micro-batch `micro` of n_micro into the fp32
+ * shard accumulators (which become the averaged gradient on the last one):
+ * s = rank-order sum; micro 0: acc = s; middle: acc = acc + s; last:
+ * acc = (acc + s) / (N_d * n_micro * loss_scale), with norm partials and the
+ * non-finite flag.  n_micro = 1 is zero_reduce_scatter.  Every bucket (unit)
+ * is reduced once per micro-batch.  Stages 2-3 (ZERO_ERR_STATE otherwise). */
+zero_status_t zero_reduce_scatter_micro(const zero_layout* L, int32_t bucket_or_unit, int32_t micro,
+                                        int32_t n_micro, const void* const* grad_replicas, float* const* acc_shards,
+                                        zero_step_state* st, void* workspace, zero_stream_t stream);
+
 /* Largest Psi_pad that zero_fused_step_noalloc accepts (64 Mi elements). */
 #define ZERO_NOALLOC_MAX_ELEMS 67108864
 

@@ -227,6 +227,22 @@ def comm_volume_elems(psi, n_d: int, stage: int) -> dict:
     return parts
 
 
+def comm_volume_micro(psi, n_d: int, stage: int, n_micro: int) -> dict:
+    """Per-rank volume of one optimizer step over n_micro micro-batches
+    (reading notes §4.1-§4.3): ZeRO-1 needs no extra communication (one
+    reduce-scatter and one all-gather per step); ZeRO-2 reduce-scatters every
+    micro-batch; ZeRO-3 all-gathers forward and backward and reduce-scatters
+    every micro-batch; DDP (stage 0) accumulates locally and all-reduces once."""
+    one = comm_volume_elems(psi, n_d, stage)
+    parts = {k: v for k, v in one.items() if k != "total"}
+    if stage == 2:
+        parts["reduce_scatter"] *= n_micro
+    elif stage == 3:
+        parts = {k: v * n_micro for k, v in parts.items()}
+    parts["total"] = sum(parts.values())
+    return parts
+
+
 def layout_comm_elems(L: Layout) -> dict:
     """Integer per-rank counters for this layout: (N_d - 1) * S per collective."""
     one = (L.n_d - 1) * L.shard_len

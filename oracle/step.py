@@ -83,6 +83,10 @@ def lib():
         L.orc_sumsq_chunks128.argtypes = [P, i64, P]; L.orc_sumsq_chunks128.restype = None
         L.orc_sum_sequential.argtypes = [P, i64]; L.orc_sum_sequential.restype = ctypes.c_double
         L.orc_adamw.argtypes = [i64, P, P, P, P, ctypes.POINTER(_Consts)]; L.orc_adamw.restype = None
+        L.orc_accumulate.argtypes = [i64, P, i32, P, i32]; L.orc_accumulate.restype = None
+        L.orc_reduce_f32.argtypes = [i32, P, i64, f32, P, P]; L.orc_reduce_f32.restype = None
+        L.orc_reduce_accumulate.argtypes = [i32, P, i32, i64, P, i32, f32, P]
+        L.orc_reduce_accumulate.restype = None
         L.orc_num_threads.argtypes = []; L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]; L.orc_set_num_threads.restype = None
         _LIB = L
@@ -122,6 +126,34 @@ def reduce_grads(reps: Sequence[np.ndarray], fmt: int, D: float) -> Tuple[np.nda
     flag = ctypes.c_int32(0)
     lib().orc_reduce(len(reps), arr, fmt, n, float(np.float32(D)), _ptr(g), ctypes.byref(flag))
     return g, bool(flag.value)
+
+
+def accumulate(x: np.ndarray, fmt: int, acc: np.ndarray, first: bool) -> None:
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"] and acc.size == x.size
+    lib().orc_accumulate(x.size, _ptr(x), fmt, _ptr(acc), int(first))
+
+
+def reduce_f32(accs: Sequence[np.ndarray], D: float) -> Tuple[np.ndarray, bool]:
+    accs = [np.ascontiguousarray(a, dtype=np.float32) for a in accs]
+    n = accs[0].size
+    arr = (ctypes.c_void_p * len(accs))(*[_ptr(a) for a in accs])
+    g = np.empty(n, np.float32)
+    flag = ctypes.c_int32(0)
+    lib().orc_reduce_f32(len(accs), arr, n, float(np.float32(D)), _ptr(g), ctypes.byref(flag))
+    return g, bool(flag.value)
+
+
+def reduce_accumulate(reps: Sequence[np.ndarray], fmt: int, acc: np.ndarray, mode: int, D: float) -> bool:
+    """mode 1: acc = s; 2: acc += s; 3: acc = (acc + s) / D.  Returns the
+    non-finite flag (mode 3 only)."""
+    reps = [np.ascontiguousarray(r, dtype=np.uint16) for r in reps]
+    assert acc.dtype == np.float32 and acc.flags["C_CONTIGUOUS"] and acc.size == reps[0].size
+    arr = (ctypes.c_void_p * len(reps))(*[_ptr(r) for r in reps])
+    flag = ctypes.c_int32(0)
+    lib().orc_reduce_accumulate(len(reps), arr, fmt, acc.size, _ptr(acc), mode, float(np.float32(D)),
+                                ctypes.byref(flag))
+    return bool(flag.value)
 
 
 def sumsq_chunks(g: np.ndarray) -> np.ndarray:
@@ -386,6 +418,71 @@ class ZeroSimulation:
             p16 = [cast16(self.master[r], self.fmt) for r in range(L.n_d)]
             if L.stage == 3:
                 self.shard16 = p16          # no all-gather at the end of the step
+            else:
+                self._allgather(p16)
+        return dict(st.history[-1])
+
+    # -- gradient accumulation over micro-batches ---------------------------------
+    def step_accumulated(self, micro_reps: Sequence[Sequence[np.ndarray]], clip_override=None) -> dict:
+        """One optimizer step over M micro-batches (micro_reps[m][r] = rank r's
+        16-bit gradient replica of micro-batch m).  Readings of the reading
+        notes §4.1-§4.3:
+          ZeRO-1 keeps full fp32 accumulators and communicates nothing until
+            the last micro-batch: A_r = x_{r,0} + x_{r,1} + ... (per rank),
+            then g = (A_0 + A_1 + ...) / (N_d * M * loss_scale);
+          ZeRO-2/3 reduce-scatter every micro-batch into the fp32 shard:
+            acc = s_0 + s_1 + ... with s_m the rank-order sum of micro-batch
+            m, then g = acc / (N_d * M * loss_scale);
+          ZeRO-3 also gathers every unit forward and backward per micro-batch.
+        M = 1 is the plain step."""
+        L, st = self.L, self.state
+        M = len(micro_reps)
+        if M == 1:
+            return self.step(micro_reps[0], clip_override)
+        D = _f32(L.n_d * M * st.loss_scale)
+        bad = False
+        if L.stage == 1:
+            accs = [np.empty(L.psi_pad, np.float32) for _ in range(L.n_d)]
+            for m, reps in enumerate(micro_reps):
+                for r in range(L.n_d):
+                    accumulate(reps[r], self.fmt, accs[r], m == 0)
+            for (b0, b1) in reversed(L.buckets):
+                u = L.units[0]
+                for r in range(L.n_d):
+                    lo, hi = max(b0, r * u.shard), min(b1, (r + 1) * u.shard)
+                    if lo >= hi:
+                        continue
+                    g, b = reduce_f32([a[lo:hi] for a in accs], D)
+                    self.gshard[r][lo - r * u.shard:hi - r * u.shard] = g
+                    bad = bad or b
+        else:
+            for m, reps in enumerate(micro_reps):
+                mode = 1 if m == 0 else (3 if m == M - 1 else 2)
+                if L.stage == 3:
+                    for ui in range(len(L.units)):
+                        self.gather_unit(ui)
+                    units = list(reversed(range(len(L.units))))
+                    ranges = [(L.units[ui].offset, L.units[ui].offset + L.units[ui].padded) for ui in units]
+                else:
+                    ranges = list(reversed(L.buckets))
+                for (b0, b1) in ranges:
+                    for u in L.units:
+                        for r in range(L.n_d):
+                            lo = max(b0, u.offset + r * u.shard)
+                            hi = min(b1, u.offset + (r + 1) * u.shard)
+                            if lo >= hi:
+                                continue
+                            j0 = u.shard_base + (lo - u.offset - r * u.shard)
+                            acc = self.gshard[r][j0:j0 + (hi - lo)]
+                            bad = reduce_accumulate([rep[lo:hi] for rep in reps], self.fmt, acc, mode, D) or bad
+        sumsq = self._global_sumsq() if not bad else math.inf
+        apply, norm, clip = st.decide(bad, sumsq, self.max_norm, clip_override)
+        if apply:
+            for r in range(L.n_d):
+                adamw_inplace(self.master[r], self.m[r], self.v[r], self.gshard[r], self.hp, st.t, clip)
+            p16 = [cast16(self.master[r], self.fmt) for r in range(L.n_d)]
+            if L.stage == 3:
+                self.shard16 = p16
             else:
                 self._allgather(p16)
         return dict(st.history[-1])

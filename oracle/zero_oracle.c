@@ -144,6 +144,63 @@ void orc_reduce(int32_t nd, const uint16_t* const* rep, int32_t fmt, int64_t n,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradient accumulation over micro-batches.                                 */
+/* ------------------------------------------------------------------------ */
+
+/* ZeRO-1 local accumulation (no communication): for one rank's 16-bit
+ * micro-batch gradient x, acc[i] = x[i] on the first micro-batch, else
+ * acc[i] = acc[i] + x[i] (binary32). */
+void orc_accumulate(int64_t n, const uint16_t* x, int32_t fmt, float* acc, int32_t first) {
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i) {
+        float xi = orc_decode(x[i], fmt);
+        acc[i] = first ? xi : acc[i] + xi;
+    }
+}
+
+/* Reduce of fp32 accumulators (ZeRO-1 after the last micro-batch):
+ * s = a_0 + a_1 + ... in rank order, g = s / D. */
+void orc_reduce_f32(int32_t nd, const float* const* acc, int64_t n, float D, float* g, int32_t* nonfinite) {
+    int32_t bad = 0;
+    int64_t i;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (i = 0; i < n; ++i) {
+        float s = acc[0][i];
+        for (int32_t r = 1; r < nd; ++r) s = s + acc[r][i];
+        if (!isfinite(s)) bad = 1;
+        g[i] = s / D;
+    }
+    if (bad) *nonfinite = 1;
+}
+
+/* ZeRO-2/3 per-micro-batch reduce-scatter into the fp32 shard accumulator:
+ * s = x_0 + ... + x_{nd-1} in rank order, then
+ *   mode 1 (first):  acc = s
+ *   mode 2 (middle): acc = acc + s
+ *   mode 3 (last):   acc = (acc + s) / D   (the averaged gradient)  */
+void orc_reduce_accumulate(int32_t nd, const uint16_t* const* rep, int32_t fmt, int64_t n, float* acc,
+                           int32_t mode, float D, int32_t* nonfinite) {
+    int32_t bad = 0;
+    int64_t i;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (i = 0; i < n; ++i) {
+        float s = orc_decode(rep[0][i], fmt);
+        for (int32_t r = 1; r < nd; ++r) s = s + orc_decode(rep[r][i], fmt);
+        if (mode == 1) {
+            acc[i] = s;
+        } else if (mode == 2) {
+            acc[i] = acc[i] + s;
+        } else {
+            float t = acc[i] + s;
+            if (!isfinite(t)) bad = 1;
+            acc[i] = t / D;
+        }
+    }
+    if (bad) *nonfinite = 1;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Global gradient norm pieces.                                              */
 /* ------------------------------------------------------------------------ */
 

@@ -37,7 +37,9 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_layout_tensor_offset", "zero_layout_destroy", "zero_state_init",
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
             "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
-            "zero_fused_step_noalloc", "zero_reshard_plan", "zero_last_error", "zero_launch_count"]
+            "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
+            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_last_error",
+            "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
 
@@ -110,6 +112,9 @@ def lib():
         "zero_fused_step": [P, i32, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P, P],
         "zero_fused_step_noalloc": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
         "zero_reshard_plan": [P, P, ctypes.POINTER(zero_copy_segment), i64, ctypes.POINTER(i64)],
+        "zero_accumulate_grads": [P, i32, PP, PP, P],
+        "zero_reduce_scatter_accumulated": [P, i32, PP, PP, i32, P, P, P],
+        "zero_reduce_scatter_micro": [P, i32, i32, i32, PP, PP, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -264,6 +269,22 @@ def zero_reshard_plan(src: Layout, dst: Layout):
     arr = (zero_copy_segment * max(1, n.value))()
     _check(lib().zero_reshard_plan(src, dst, arr, n.value, ctypes.byref(n)))
     return [(g.src_rank, g.src_off, g.dst_rank, g.dst_off, g.len) for g in arr[:n.value]]
+
+
+def zero_accumulate_grads(L: Layout, micro: int, grad_replicas, acc_replicas, stream=None) -> None:
+    _check(lib().zero_accumulate_grads(L, micro, _ptrs(grad_replicas), _ptrs(acc_replicas), _stream(stream)))
+
+
+def zero_reduce_scatter_accumulated(L: Layout, bucket: int, acc_replicas, grad_shards, n_micro: int, st, workspace,
+                                    stream=None) -> None:
+    _check(lib().zero_reduce_scatter_accumulated(L, bucket, _ptrs(acc_replicas), _ptrs(grad_shards), n_micro,
+                                                 _addr(st), _addr(workspace), _stream(stream)))
+
+
+def zero_reduce_scatter_micro(L: Layout, bucket_or_unit: int, micro: int, n_micro: int, grad_replicas, acc_shards,
+                              st, workspace, stream=None) -> None:
+    _check(lib().zero_reduce_scatter_micro(L, bucket_or_unit, micro, n_micro, _ptrs(grad_replicas),
+                                           _ptrs(acc_shards), _addr(st), _addr(workspace), _stream(stream)))
 
 
 def zero_last_error() -> str:

@@ -32,12 +32,12 @@ struct AdamTmaSmem {
     static constexpr size_t total = bar_off + (size_t)STAGES * sizeof(uint64_t);
 };
 
-template <int ND, class F, int OUT, int TE, int STAGES, int OSTAGES>
-__global__ void __launch_bounds__(kThreads, 1) adamw_tma_kernel(const __grid_constant__ AdamArgs a) {
+template <int ND, class F, int OUT, int TE, int STAGES, int OSTAGES, int NT>
+__global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant__ AdamArgs a) {
     using SM = AdamTmaSmem<TE, STAGES, OSTAGES>;
     constexpr int OST = SM::kOst;
-    constexpr int PARTS = TE / (kThreads * 4);  // float4 groups per thread per tile
-    static_assert(PARTS >= 1 && TE % (kThreads * 4) == 0, "tile must give every thread whole float4 groups");
+    constexpr int PARTS = TE / (NT * 4);  // float4 groups per thread per tile
+    static_assert(PARTS >= 1 && TE % (NT * 4) == 0, "tile must give every thread whole float4 groups");
     extern __shared__ __align__(1024) unsigned char smem[];
     float* in = reinterpret_cast<float*>(smem);
     float* ob = reinterpret_cast<float*>(smem + SM::in_bytes);
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) adamw_tma_kernel(const __grid_con
         if (ok) {
 #pragma unroll
             for (int part = 0; part < PARTS; ++part) {
-                const int e = part * kThreads * 4 + tid * 4;
+                const int e = part * NT * 4 + tid * 4;
                 if ((uint32_t)e < len) {
                     const float4 g4 = *reinterpret_cast<const float4*>(src + e);
                     float4 p4 = *reinterpret_cast<const float4*>(src + TE + e);
@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
 using namespace zero_detail;
 
 template <class Kernel>
-static zero_status_t launch_tma(Kernel kern, size_t smem, int64_t tiles, const zk::AdamArgs& a, cudaStream_t s) {
+static zero_status_t launch_tma(Kernel kern, size_t smem, int64_t tiles, const zk::AdamArgs& a, cudaStream_t s,
+                                int threads) {
     static std::mutex mu;
     static std::unordered_map<const void*, int> configured;
     {
@@ -231,8 +232,8 @@ static zero_status_t launch_tma(Kernel kern, size_t smem, int64_t tiles, const z
             configured[reinterpret_cast<const void*>(kern)] = 1;
         }
     }
-    const int grid = persistent_grid(kern, tiles, smem);
-    kern<<<grid, zk::kThreads, smem, s>>>(a);
+    const int grid = persistent_grid(kern, tiles, smem, threads);
+    kern<<<grid, threads, smem, s>>>(a);
     return after_launch("zero_adamw_shard_step");
 }
 
@@ -240,13 +241,21 @@ template <int ND, class F, int OUT, int TE, int STAGES, int OST>
 static zero_status_t launch_adamw_tma(const zk::AdamArgs& a, cudaStream_t s) {
     const int64_t S = (int64_t)a.shard_v * zk::kVec;
     const int64_t tiles = ((S + TE - 1) / TE) * a.nd;
-    return launch_tma(zk::adamw_tma_kernel<ND, F, OUT, TE, STAGES, OST>, zk::AdamTmaSmem<TE, STAGES, OST>::total,
-                      tiles, a, s);
+    // With few bytes per element (16-bit shard output, or at most 4 replicas)
+    // the update is bound by instruction latency, and 16 warps per SM beat 8
+    // (7B ZeRO-3 shard update 50.2 -> 43.9 ms); with 8 replicas it is bound by
+    // bandwidth and 8 warps are faster (10.99 vs 11.38 ms at 1.5B).
+    if (OUT == ZERO_OUT_SHARDS || a.nd <= 4)
+        return launch_tma(zk::adamw_tma_kernel<ND, F, OUT, TE, STAGES, OST, 512>,
+                          zk::AdamTmaSmem<TE, STAGES, OST>::total, tiles, a, s, 512);
+    return launch_tma(zk::adamw_tma_kernel<ND, F, OUT, TE, STAGES, OST, 256>, zk::AdamTmaSmem<TE, STAGES, OST>::total,
+                      tiles, a, s, 256);
 }
 
 // Tile 2048 elements, 4 load stages, 2 output stages (188 KB of shared
 // memory, one CTA per SM): on GB300 this shape reaches 98% of the bandwidth a
-// plain streaming kernel gets for the same 16-byte-read / 28-byte-write mix.
+// plain streaming kernel gets for the 16-byte-read / 28-byte-write mix of the
+// 8-replica update.
 template <int ND, class F>
 static zero_status_t launch_adamw(const zk::AdamArgs& a, int out_kind, cudaStream_t s) {
     if (out_kind == ZERO_OUT_FULL_REPLICAS) return launch_adamw_tma<ND, F, ZERO_OUT_FULL_REPLICAS, 2048, 4, 2>(a, s);

@@ -364,6 +364,29 @@ struct RsArgs {
     zero_step_state* st;
     SegArgs seg;
     int32_t nd;
+    int32_t n_micro;  // micro-batches of the step (1: plain reduce-scatter)
+};
+
+// Reduce-scatter modes: plain, and the first / middle / last micro-batch of
+// an accumulated step.
+enum { RS_PLAIN = 0, RS_FIRST = 1, RS_MIDDLE = 2, RS_LAST = 3 };
+
+struct AccumArgs {
+    const uint16_t* rep[kMaxRanks];
+    float* acc[kMaxRanks];
+    uint32_t v_per_rank;  // Psi_pad / 8
+    int64_t real_end;     // padding starts here
+    int32_t nd;
+};
+
+struct RsAccArgs {
+    const float* acc[kMaxRanks];
+    float* gshard[kMaxRanks];
+    float* partials;
+    zero_step_state* st;
+    SegArgs seg;
+    int32_t nd;
+    int32_t n_micro;
 };
 
 struct AdamArgs {

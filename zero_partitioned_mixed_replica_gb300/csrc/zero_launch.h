@@ -28,7 +28,7 @@ inline int sm_count() {
 // Persistent grid: every CTA resident at once (SMs x resident CTAs per SM),
 // capped by the CTAs the work needs; kernels grid-stride over the rest.
 template <class Kernel>
-inline int persistent_grid(Kernel kernel, int64_t work_ctas, size_t dyn_smem = 0) {
+inline int persistent_grid(Kernel kernel, int64_t work_ctas, size_t dyn_smem = 0, int threads = zk::kThreads) {
     // resident CTAs per SM, cached per (device, kernel address)
     static std::mutex mu;
     static std::unordered_map<const void*, int> cache[64];
@@ -42,7 +42,7 @@ inline int persistent_grid(Kernel kernel, int64_t work_ctas, size_t dyn_smem = 0
         if (it != cache[dev].end()) per_sm = it->second;
     }
     if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, zk::kThreads, dyn_smem) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) != cudaSuccess ||
             per_sm <= 0)
             per_sm = 1;
         std::lock_guard<std::mutex> lock(mu);

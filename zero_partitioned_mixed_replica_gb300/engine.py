@@ -52,7 +52,7 @@ class ZeroStep:
                  adamw: AdamW = AdamW(), max_norm: float = 0.0, loss_scale: float = 1.0,
                  dynamic_scale: bool = False, growth_interval: int = 2000,
                  fused: Optional[bool] = None, per_bucket: bool = True, fuse_allgather: bool = True,
-                 device: str = "cuda", stream: Optional[torch.cuda.Stream] = None):
+                 n_micro: int = 1, device: str = "cuda", stream: Optional[torch.cuda.Stream] = None):
         if stage not in (1, 2, 3):
             raise ValueError("ZeroStep runs ZeRO stages 1, 2 and 3")
         self.L = B.zero_layout_init(list(numels), list(unit_of_tensor) if unit_of_tensor is not None else None,
@@ -64,7 +64,12 @@ class ZeroStep:
         self.loss_scale0 = float(loss_scale)
         self.dynamic, self.growth_interval = bool(dynamic_scale), int(growth_interval)
         no_scaler = (not dynamic_scale) and loss_scale == 1.0
-        self.fused = (self.max_norm <= 0 and no_scaler) if fused is None else bool(fused)
+        self.n_micro = int(n_micro)
+        if self.n_micro < 1:
+            raise ValueError("n_micro must be >= 1")
+        self.fused = (self.max_norm <= 0 and no_scaler and self.n_micro == 1) if fused is None else bool(fused)
+        if self.fused and self.n_micro > 1:
+            raise ValueError("gradient accumulation uses the split step")
         if self.fused and not (self.max_norm <= 0 and no_scaler):
             raise ValueError("the fused step cannot clip or skip: use the split step")
         self.per_bucket = per_bucket
@@ -86,6 +91,10 @@ class ZeroStep:
         self.m = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
         self.v = torch.zeros(n_d, S, dtype=torch.float32, device=dev)
         self.gshard = None if self.fused else torch.zeros(n_d, S, dtype=torch.float32, device=dev)
+        # ZeRO-1 accumulates each rank's full gradient in fp32 ("第 5 课" §2: + 4 Psi per rank);
+        # ZeRO-2/3 accumulate in the fp32 shard itself (+ 4 Psi / N_d, already held)
+        self.acc = (torch.zeros(n_d, P, dtype=torch.float32, device=dev)
+                    if (self.n_micro > 1 and stage == 1) else None)
         if stage == 3:
             self.params = None
             self.shard16 = torch.zeros(n_d, S, dtype=dt16, device=dev)
@@ -122,6 +131,7 @@ class ZeroStep:
         self.param_rows = rows(self.params)
         self.shard16_rows = rows(self.shard16)
         self.transient_rows = rows(self.transient)
+        self.acc_rows = rows(getattr(self, "acc", None))
 
     def _s(self):
         return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
@@ -217,6 +227,54 @@ class ZeroStep:
                 C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
                   self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
                 C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
+
+    # -- gradient accumulation over micro-batches ------------------------------------
+    def micro_step(self, micro: int) -> None:
+        """Process micro-batch ``micro`` (0-based) of ``n_micro``, whose 16-bit
+        gradients are in ``grads``; the last one finishes the optimizer step.
+        ZeRO-1 accumulates locally in fp32 and reduce-scatters once (reading
+        notes §4.1); ZeRO-2 reduce-scatters every micro-batch into the fp32
+        shard (§4.2); ZeRO-3 also gathers every unit forward and backward for
+        every micro-batch (§4.3)."""
+        M = self.n_micro
+        if M == 1:
+            self.step()
+            return
+        if not 0 <= micro < M:
+            raise ValueError("micro out of range")
+        s = self._s()
+        L, C = self.L, self._call
+        last = micro == M - 1
+        if self.stage == 1:
+            C("accumulate", B.zero_accumulate_grads, L, micro, self.grad_rows, self.acc_rows, s)
+            if not last:
+                return
+            for b in reversed(range(self.n_buckets)):
+                C("reduce_scatter", B.zero_reduce_scatter_accumulated, L, b, self.acc_rows, self.gshard_rows, M,
+                  self.state, self.workspace, s)
+        elif self.stage == 2:
+            for b in reversed(range(self.n_buckets)):
+                C("reduce_scatter", B.zero_reduce_scatter_micro, L, b, micro, M, self.grad_rows, self.gshard_rows,
+                  self.state, self.workspace, s)
+            if not last:
+                return
+        else:
+            U = len(self.units)
+            for u in range(U):
+                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
+            for u in reversed(range(U)):
+                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
+                C("reduce_scatter", B.zero_reduce_scatter_micro, L, u, micro, M, self.grad_rows, self.gshard_rows,
+                  self.state, self.workspace, s)
+            if not last:
+                return
+        C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
+        out = self.shard16_rows if (self.stage == 3 or not self.fuse_allgather) else self.param_rows
+        kind = B.ZERO_OUT_SHARDS if out is self.shard16_rows else B.ZERO_OUT_FULL_REPLICAS
+        C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
+          self.gshard_rows, self.state, out, kind, s)
+        if self.stage != 3 and not self.fuse_allgather:
+            C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
 
     # -- CUDA graph of one step -------------------------------------------------------
     def capture(self) -> torch.cuda.CUDAGraph:
