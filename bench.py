@@ -59,6 +59,11 @@ def parse():
     p.add_argument("--sweep-nd", default="2,4,8,16,64")
     p.add_argument("--micro", type=int, default=1,
                    help="micro-batches per optimizer step (gradient accumulation, split step)")
+    p.add_argument("--prefetch", action="store_true",
+                   help="ZeRO-3: gathers on a second stream under a stand-in per-unit GEMM (one JSON line)")
+    p.add_argument("--comm-ctas", type=int, default=0, help="prefetch: CTA cap of the library's launches")
+    p.add_argument("--compute-tokens", type=int, default=8192,
+                   help="rows of the stand-in GEMM [tokens x d] x [d x d] per unit and pass")
     p.add_argument("--checkpoint", default="",
                    help="directory: time a sharded checkpoint save and a load resharded to N_d/2 (one JSON line)")
     return p.parse_args()
@@ -421,8 +426,68 @@ def checkpoint_bench(args):
                       "segments": info["segments"]}), flush=True)
 
 
+def prefetch_bench(args):
+    """ZeRO-3 forward/backward prefetch: each unit's forward and backward is
+    stood in for by one bf16 GEMM [tokens x d] x [d x d] on the compute stream
+    (d = the model width, the weight being the first d x d block of the
+    gathered unit); the unit gathers (and, in backward, the unit's
+    reduce-scatter + update) run on a second stream.  Reports the step time
+    with 1 live unit (no prefetch) and 2 (prefetch), the compute-only and
+    communication-only times, and the fraction of the smaller one hidden."""
+    import torch
+    from zero_partitioned_mixed_replica_gb300 import build as zbuild
+    from zero_partitioned_mixed_replica_gb300 import synth, workloads
+    from zero_partitioned_mixed_replica_gb300.engine import ZeroStep
+    zbuild.build()
+    w = workloads.ALL[args.workload]()
+    assert w.stage == 3, "prefetch needs a ZeRO-3 workload"
+    dev = torch.device("cuda", 0)
+    eng = ZeroStep(w.numels, w.n_d, 3, w.dtype, 0, w.unit_of_tensor, device=str(dev))
+    eng.load_master(synth.master_init(w.numels, eng.tensor_offsets, eng.info.psi_pad, device=dev))
+    synth.grad_replica(w.numels, eng.tensor_offsets, eng.info.psi_pad, w.dtype, 0, 1, w.grad_std,
+                       device=dev, out=eng.grads[0])
+    for r in range(1, w.n_d):
+        eng.grads[r].copy_(eng.grads[0])
+    d = 4096 if w.numels[0] % 4096 == 0 else 1600   # model width of the Llama / GPT-2 1.5B layouts
+    x = torch.randn(args.compute_tokens, d, device=dev, dtype=torch.bfloat16)
+    y = torch.empty(args.compute_tokens, d, device=dev, dtype=torch.bfloat16)
+
+    def compute(kind, u, rows):
+        wgt = rows[0][:d * d].view(d, d)
+        torch.matmul(x, wgt, out=y)
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    U = len(eng.units)
+    reps = max(1, args.steps)
+    t_seq = timed(lambda: eng.step_overlapped(compute, 1), reps)
+    t_ovl = timed(lambda: eng.step_overlapped(compute, 2, args.comm_ctas), reps)
+    t_comp = timed(lambda: [compute("fwd", u, [eng.transient[r] for r in range(w.n_d)]) for u in range(2 * U)],
+                   reps)
+    t_comm = timed(eng.step, reps)
+    hidden = (t_seq - t_ovl) / min(t_comp, t_comm)
+    print(json.dumps({"prefetch": w.name, "units": U, "compute_tokens": args.compute_tokens, "gemm_d": d,
+                      "comm_ctas": args.comm_ctas,
+                      "ms_no_prefetch": t_seq, "ms_prefetch": t_ovl, "ms_compute_only": t_comp,
+                      "ms_comm_only": t_comm, "hidden_fraction": hidden,
+                      "t_compute_ge_t_comm": t_comp >= t_comm}), flush=True)
+
+
 def main():
     args = parse()
+    if args.prefetch:
+        prefetch_bench(args)
+        return
     if args.sweep:
         sweep(args)
         return

@@ -385,6 +385,14 @@ zero_status_t zero_fused_step_noalloc(const zero_layout* L, const zero_adamw_hp*
                                       void* const* param16_out, int32_t out_kind,
                                       zero_stream_t stream);
 
+/* Cap on the CTAs of every later launch by this library (process-wide;
+ * 0 = no cap: persistent grids of one full wave of CTAs).  For overlapping
+ * the library's memory-bound kernels with other work on another stream
+ * (ZeRO-3 prefetch under a layer's compute): a full-wave grid occupies every
+ * SM, so concurrent kernels would serialise behind it.  Results do not depend
+ * on the cap.  Returns the previous value. */
+int32_t zero_set_max_ctas(int32_t max_ctas);
+
 /* Message for the last failing call on this thread ("" if none). */
 const char* zero_last_error(void);
 

@@ -38,8 +38,8 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
             "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
-            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_last_error",
-            "zero_launch_count"]
+            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_set_max_ctas",
+            "zero_last_error", "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
 
@@ -126,6 +126,8 @@ def lib():
     L.zero_last_error.restype = ctypes.c_char_p
     L.zero_launch_count.argtypes = [i32]
     L.zero_launch_count.restype = i64
+    L.zero_set_max_ctas.argtypes = [i32]
+    L.zero_set_max_ctas.restype = i32
     _lib = L
     return L
 
@@ -285,6 +287,10 @@ def zero_reduce_scatter_micro(L: Layout, bucket_or_unit: int, micro: int, n_micr
                               st, workspace, stream=None) -> None:
     _check(lib().zero_reduce_scatter_micro(L, bucket_or_unit, micro, n_micro, _ptrs(grad_replicas),
                                            _ptrs(acc_shards), _addr(st), _addr(workspace), _stream(stream)))
+
+
+def zero_set_max_ctas(n: int) -> int:
+    return int(lib().zero_set_max_ctas(int(n)))
 
 
 def zero_last_error() -> str:

@@ -40,4 +40,5 @@ int64_t workspace_bytes(const zero_layout* L);
 zero_status_t fail(zero_status_t code, const std::string& msg);
 void clear_error();
 void count_launches(int64_t n);
+int32_t max_ctas();
 }  // namespace zero_detail

@@ -51,6 +51,8 @@ inline int persistent_grid(Kernel kernel, int64_t work_ctas, size_t dyn_smem = 0
     int sms = sm_count();
     if (sms <= 0) sms = 1;
     int64_t cap = (int64_t)sms * per_sm;
+    const int32_t user_cap = max_ctas();
+    if (user_cap > 0 && user_cap < cap) cap = user_cap;
     int64_t g = work_ctas < cap ? work_ctas : cap;
     return g < 1 ? 1 : (int)g;
 }

@@ -9,6 +9,7 @@
 // FSDP", FSDP section.  Memory M0..M3: "第 5 课" §2.  Volumes (N_d - 1)/N_d Psi
 // per collective: "第 5 课" §3, reading notes §6.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <new>
 
@@ -28,6 +29,9 @@ void clear_error() { g_last_error.clear(); }
 
 void count_launches(int64_t n) { g_launches += n; }
 
+static std::atomic<int32_t> g_max_ctas{0};
+int32_t max_ctas() { return g_max_ctas.load(std::memory_order_relaxed); }
+
 int64_t partials_count(const zero_layout* L) { return L->psi_pad / kGroup; }
 
 static int64_t round_up(int64_t x, int64_t m) { return ((x + m - 1) / m) * m; }
@@ -42,6 +46,10 @@ int64_t workspace_bytes(const zero_layout* L) {
 using namespace zero_detail;
 
 extern "C" const char* zero_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int32_t zero_set_max_ctas(int32_t n) {
+    return g_max_ctas.exchange(n < 0 ? 0 : n, std::memory_order_relaxed);
+}
 
 extern "C" int64_t zero_launch_count(int32_t reset) {
     int64_t n = g_launches;

@@ -228,6 +228,61 @@ class ZeroStep:
                   self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
                 C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
 
+    # -- ZeRO-3 prefetch: gathers on a second stream overlap the layers' compute -------
+    def step_overlapped(self, compute, max_live_units: int = 2, comm_ctas: int = 0) -> None:
+        """ZeRO-3 step whose unit gathers run on a communication stream while
+        ``compute(kind, unit, transient_rows)`` — the caller's stand-in for
+        the layer's forward ("fwd") or backward ("bwd") work, launched on the
+        current stream — uses the previous unit ("第 5 课：ZeRO 与 FSDP" §4:
+        gather layer l+1 in forward and l-1 in backward while layer l
+        computes; "ZeRO-3 核心流程" §3; reading notes §4.3).  In backward the
+        unit's reduce-scatter and update follow its compute on the
+        communication stream.  ``max_live_units`` transient buffers are in
+        flight (1 = no prefetch: every gather waits for the previous
+        compute).  ``comm_ctas`` > 0 caps the CTAs of the library's launches
+        in this step, leaving SMs to the concurrent compute.  Results are
+        identical to :meth:`step`."""
+        if self.stage != 3 or not self.fused:
+            raise ValueError("step_overlapped runs the fused ZeRO-3 step")
+        nb = max(1, int(max_live_units))
+        if getattr(self, "_bufs", None) is None or len(self._bufs) < nb:
+            self._bufs = [self.transient] + [torch.zeros_like(self.transient) for _ in range(nb - 1)]
+            self._comm = torch.cuda.Stream(self.device)
+        comp = self._s()
+        comm = self._comm
+        L, U = self.L, len(self.units)
+        uses = [("fwd", u) for u in range(U)] + [("bwd", u) for u in reversed(range(U))]
+        gathered = [torch.cuda.Event() for _ in uses]
+        used = [torch.cuda.Event() for _ in uses]
+        rows = [[b[r] for r in range(self.n_d)] for b in self._bufs[:nb]]
+        comm.wait_stream(comp)
+        prev_cap = B.zero_set_max_ctas(comm_ctas) if comm_ctas > 0 else None
+
+        def gather(i):
+            kind, u = uses[i]
+            if i >= nb:
+                comm.wait_event(used[i - nb])       # its buffer's previous user is done
+            B.zero_stage3_gather_layer(L, u, self.shard16_rows, rows[i % nb], comm)
+            gathered[i].record(comm)
+
+        gather(0)
+        for i, (kind, u) in enumerate(uses):
+            if i + 1 < len(uses) and nb > 1:
+                gather(i + 1)                        # prefetch the next unit
+            comp.wait_event(gathered[i])
+            compute(kind, u, rows[i % nb])
+            used[i].record(comp)
+            if nb == 1 and i + 1 < len(uses):
+                gather(i + 1)
+            if kind == "bwd":
+                comm.wait_event(used[i])             # the unit's gradients exist after its backward
+                B.zero_fused_step(L, u, self.hp, self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
+                                  self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, self.workspace, comm)
+        B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, comm)
+        comp.wait_stream(comm)
+        if prev_cap is not None:
+            B.zero_set_max_ctas(prev_cap)
+
     # -- gradient accumulation over micro-batches ------------------------------------
     def micro_step(self, micro: int) -> None:
         """Process micro-batch ``micro`` (0-based) of ``n_micro``, whose 16-bit
