@@ -329,7 +329,7 @@ def gpu_run(args, w, rank, world, local_rank):
             a.record(stream)
             for _ in range(args.e2e_steps):
                 for mb in range(args.micro):
-                    eng.grads.copy_(host_grads, non_blocking=True)
+                    eng.upload_grads(host_grads)
                     eng.micro_step(mb)
                 host_state.copy_(eng.state, non_blocking=True)
             b.record(stream)

@@ -348,6 +348,24 @@ class ZeroStep:
         torch.cuda.current_stream(self.device).wait_stream(side)
         return g
 
+    # -- host input ----------------------------------------------------------------------
+    def upload_grads(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
+        """Copy the N_d gradient replicas from (pinned) host memory, in chunks
+        alternating over two copy streams (faster than one large copy on this
+        part), ordered before the next library call on the step's stream."""
+        assert tuple(host.shape) == tuple(self.grads.shape) and host.dtype == self.grads.dtype
+        if getattr(self, "_copy_streams", None) is None:
+            self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
+        cur = self._s()
+        flat_h, flat_d = host.view(-1), self.grads.view(-1)
+        for s in self._copy_streams:
+            s.wait_stream(cur)
+        for i, off in enumerate(range(0, flat_h.numel(), chunk_elems)):
+            with torch.cuda.stream(self._copy_streams[i % 2]):
+                flat_d[off:off + chunk_elems].copy_(flat_h[off:off + chunk_elems], non_blocking=True)
+        for s in self._copy_streams:
+            cur.wait_stream(s)
+
     # -- sharded checkpoints ("別再複製本可分片的東西：ZeRO 與 FSDP": each rank dumps
     #    its own shard in parallel) ---------------------------------------------------
     def _shard16_rows_view(self):
