@@ -375,20 +375,29 @@ def sweep(args):
                     eng.step()
                 torch.cuda.synchronize(dev)
                 B.zero_launch_count(reset=True)
+                for _ in range(args.steps):   # launch count of eager steps
+                    eng.step()
+                torch.cuda.synchronize(dev)
+                launches = B.zero_launch_count() // args.steps
+                graph = eng.capture() if args.graph else None
+                run = graph.replay if graph is not None else eng.step
+                run()
+                torch.cuda.synchronize(dev)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 for _ in range(args.steps):
-                    eng.step()
+                    run()
                 e1.record()
                 torch.cuda.synchronize(dev)
                 ms = e0.elapsed_time(e1) / args.steps
+                del graph
                 print(json.dumps({"sweep": "gpt2_medium_350M+1", "n_d": nd, "stage": stage,
                                   "bucket_elems": b if stage != 3 else "per unit",
                                   "n_buckets": eng.n_buckets if stage != 3 else len(eng.units),
                                   "ms_per_step": ms, "params_per_s": w.psi / (ms / 1e3),
                                   "hbm_gbs": bpp * eng.info.psi_pad / (ms / 1e3) / 1e9,
-                                  "bytes_per_param": bpp,
-                                  "launches_per_step": B.zero_launch_count() // args.steps}), flush=True)
+                                  "bytes_per_param": bpp, "graph": bool(args.graph),
+                                  "launches_per_step": launches}), flush=True)
             del eng
             torch.cuda.empty_cache()
 
