@@ -145,3 +145,12 @@ def test_step_calls_validate_before_launch():
     assert status(B.zero_state_init, MIS, 0.9, 0.999, 1.0, False, 10, 0) == B.ZERO_ERR_ALIGN
     assert status(B.zero_state_init, FAKE, 1.0, 0.999, 1.0, False, 10, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_state_init, FAKE, 0.9, 0.999, 0.5, False, 10, 0) == B.ZERO_ERR_INVALID
+
+
+def test_layout_rejects_psi_pad_at_the_vector_counter_limit():
+    # Psi_pad / 8 must stay below 2^31 (32-bit grid-stride counters)
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_layout_init([1 << 34], None, 1, 2, 0, 0, B.ZERO_BF16)
+    assert e.value.status == B.ZERO_ERR_INVALID
+    L = B.zero_layout_init([(1 << 34) - 1024], None, 1, 2, 0, 0, B.ZERO_BF16)
+    assert B.zero_layout_query(L).psi_pad == (1 << 34) - 1024

@@ -292,3 +292,40 @@ def test_launch_count_of_a_split_step():
     torch.cuda.synchronize()
     # one reduce-scatter per bucket, two norm passes, one AdamW
     assert Bd.zero_launch_count() == eng.n_buckets + 3
+
+
+def test_nan_gradient_skips_split_step_and_is_reported_by_fused_step():
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=1.0)
+    L = c.layout()
+    for fused in (False, True):
+        cc = Case(c.numels, c.n_d, c.stage, c.fmt, c.bucket_elems, max_norm=0.0 if fused else 1.0)
+        eng = _engine(cc)
+        eng.load_master(torch.from_numpy(cc.master0(L)))
+        before = eng.master.clone()
+        for r, g in enumerate(cc.grads_torch(L, 1, 1.0)):
+            eng.grads[r].copy_(g.cuda())
+        eng.grads[1].view(torch.int16)[L.psi // 3] = 0x7FC1          # NaN in a real element
+        eng.step()
+        st = eng.read_state()
+        assert st["overflow"] == 1 and st["nonfinite"] == 0
+        if fused:   # no global decision before the update: the step ran and t advanced
+            assert st["t"] == 1
+        else:
+            assert st["t"] == 0 and st["skipped"] == 1 and torch.equal(eng.master, before)
+
+
+def test_zero_gradients_apply_weight_decay_only():
+    c = Case([120_000, 7, 50_001], 3, 2, FMT_BF16, bucket_elems=32_768, grad_std=0.0)
+    eng, zs, _ = run_parity(c, 2)
+    assert float(eng.read_state()["grad_norm"]) == 0.0
+    assert not eng.m.any() and not eng.v.any()
+
+
+def test_units_smaller_than_a_rank_slice():
+    # 3- and 5-element units with N_d = 4: most ranks own only padding of them
+    c = Case([3, 5000, 5, 70_000], 4, 3, FMT_BF16, units=[0, 1, 2, 3])
+    run_parity(c, 2)
+    c = Case([3, 5000, 5, 70_000], 4, 3, FMT_FP16, units=[0, 1, 2, 3], max_norm=0.1, loss_scale=512.0,
+             dynamic=True)
+    run_parity(c, 2, use_gpu_clip=True)
