@@ -150,8 +150,12 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     if (tid == 0) bulk_wait_all<0>();
 }
 
+// Four CTAs of 256 threads per SM (64 registers, no spills): the shard-output
+// variant otherwise takes 68 registers and three CTAs, and at N_d = 2 its
+// ~30 B/param leave it bound by latency (7B ZeRO-3 unit update 0.977 ->
+// 0.941 ms).  Five CTAs per SM force spills.
 template <int ND, class F, int OUT>
-__global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constant__ FusedArgs a) {
     __shared__ AdamConsts sk;
     __shared__ float sD;
     const int nd = ND > 0 ? ND : a.nd;

@@ -134,6 +134,18 @@ def llama7b() -> Workload:
                     grad_std=5e-4, per_tensor_scale=False, steps=10)
 
 
+def llama7b_block() -> Workload:
+    """One Llama-style 7B block (202M parameters) as ZeRO-3 unit 1 behind a
+    4096-element root unit (the final norm), with the 7B run's settings: the
+    same per-unit gather and fused kernels on ~4 GB of device memory, small
+    enough for multi-pass profiler captures and still far above L2."""
+    numels, units = llama_tensors(n_layer=1)
+    block = numels[1:-2]
+    return Workload("one Llama-style 7B block (202M) + final norm, N_d=2, ZeRO-3 (2 units), bf16",
+                    [4096] + block, [0] + [1] * len(block), n_d=2, stage=3, dtype=BF16,
+                    bucket_elems=0, grad_std=5e-4, per_tensor_scale=False, steps=10)
+
+
 def gpt2_medium_odd(n_d: int = 8, stage: int = 2, bucket_elems: int = 5_000_000) -> Workload:
     numels, units = gpt2_tensors(24, 1024, 4096)
     numels = numels + [1]
@@ -145,5 +157,5 @@ def gpt2_medium_odd(n_d: int = 8, stage: int = 2, bucket_elems: int = 5_000_000)
 
 
 ALL = {"tiny": tiny, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl, "llama7b": llama7b,
-       "gpt2_xl_block": gpt2_xl_block,
+       "gpt2_xl_block": gpt2_xl_block, "llama7b_block": llama7b_block,
        "gpt2_medium": gpt2_medium_odd}
