@@ -328,9 +328,12 @@ def gpu_run(args, w, rank, world, local_rank):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for _ in range(args.e2e_steps):
-                for mb in range(args.micro):
-                    eng.upload_grads(host_grads)
-                    eng.micro_step(mb)
+                if args.micro == 1:
+                    eng.step_from_host(host_grads)     # per-bucket copies overlap the reduce-scatter
+                else:
+                    for mb in range(args.micro):
+                        eng.upload_grads(host_grads)
+                        eng.micro_step(mb)
                 host_state.copy_(eng.state, non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize(dev)

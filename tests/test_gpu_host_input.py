@@ -1,0 +1,53 @@
+"""Steps whose gradient replicas come from pinned host memory
+(``ZeroStep.step_from_host``): per-bucket (ZeRO-3: per-unit) copies on two
+copy streams, each reduce-scatter or fused update ordered after its own range
+only.  Checked against the oracle bit for bit, on layouts whose buckets
+straddle shards, with chunks smaller than a bucket, and against the
+device-resident step."""
+import pytest
+import torch
+
+from oracle.step import FMT_BF16, FMT_FP16
+from tests._cases import Case
+from tests.test_gpu_parity import Z3_NUMELS, Z3_UNITS, run_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from zero_partitioned_mixed_replica_gb300 import build
+    build.build()
+
+
+def test_host_input_zero2_fp16_scaler_overflow():
+    c = Case([200_000, 1600, 99_999], 8, 2, FMT_FP16, bucket_elems=65_536, max_norm=1.0,
+             loss_scale=65536.0, dynamic=True, per_tensor_scale=True, inf_step=2, inf_rank=3)
+    _, _, hist = run_parity(c, 3, use_gpu_clip=True, host_input=40_000)   # chunks smaller than a bucket
+    assert [g["overflow"] for g, _ in hist] == [0, 1, 0]
+
+
+def test_host_input_zero1_fused_per_bucket():
+    c = Case([40_000, 33, 77_777, 5], 5, 1, FMT_BF16, bucket_elems=16_384, per_tensor_scale=True)
+    run_parity(c, 2, host_input=True, per_bucket=False)   # step_from_host runs per bucket regardless
+
+
+def test_host_input_garbage_padding():
+    c = Case([100_001, 3], 3, 1, FMT_BF16)
+    run_parity(c, 2, garbage_pads=True, host_input=True)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_host_input_zero3(fused):
+    c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS, max_norm=0.0 if fused else 0.05)
+    run_parity(c, 2, host_input=10_000, use_gpu_clip=not fused)
+
+
+def test_host_input_equals_device_step():
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    e1, _, _ = run_parity(c, 2, use_gpu_clip=True, host_input=True)
+    e2, _, _ = run_parity(c, 2, use_gpu_clip=True)
+    assert torch.equal(e1.master, e2.master) and torch.equal(e1.params, e2.params)
+    assert torch.equal(e1.m, e2.m) and torch.equal(e1.v, e2.v)

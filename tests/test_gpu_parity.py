@@ -61,7 +61,7 @@ def assert_p16_close(gpu: np.ndarray, ref: np.ndarray, what: str):
 
 
 def run_parity(case: Case, steps: int, garbage_pads: bool = False, use_gpu_clip: bool = False,
-               expect_bitwise: bool = True, **engine_kw):
+               expect_bitwise: bool = True, host_input: bool = False, **engine_kw):
     L = case.layout()
     eng = _engine(case, **engine_kw)
     m0 = case.master0(L)
@@ -75,12 +75,20 @@ def run_parity(case: Case, steps: int, garbage_pads: bool = False, use_gpu_clip:
     for s in range(1, steps + 1):
         reps_t = case.grads_torch(L, s, zs.state.loss_scale)
         reps = [_u16(t) for t in reps_t]
-        for r in range(case.n_d):
-            eng.grads[r].copy_(reps_t[r].to(eng.device))
-            if garbage_pads and pad.any():
-                idx = torch.from_numpy(np.flatnonzero(pad)).to(eng.device)
-                eng.grads[r].view(torch.int16)[idx] = 0x7F81 if r % 2 else 0x7C00   # NaN / inf bits
-        eng.step()
+        if host_input:      # the replicas come from pinned host memory inside the step
+            host = torch.empty(tuple(eng.grads.shape), dtype=eng.grads.dtype, pin_memory=True)
+            for r in range(case.n_d):
+                host[r].copy_(reps_t[r])
+                if garbage_pads and pad.any():
+                    host[r].view(torch.int16)[torch.from_numpy(np.flatnonzero(pad))] = 0x7F81 if r % 2 else 0x7C00
+            eng.step_from_host(host, chunk_elems=host_input if host_input is not True else 1 << 27)
+        else:
+            for r in range(case.n_d):
+                eng.grads[r].copy_(reps_t[r].to(eng.device))
+                if garbage_pads and pad.any():
+                    idx = torch.from_numpy(np.flatnonzero(pad)).to(eng.device)
+                    eng.grads[r].view(torch.int16)[idx] = 0x7F81 if r % 2 else 0x7C00   # NaN / inf bits
+            eng.step()
         g = eng.read_state()
         o = zs.step(reps, clip_override=g["clip_coef"] if use_gpu_clip else None)
         hist.append((g, o))

@@ -177,8 +177,15 @@ class ZeroStep:
 
     # -- the step ------------------------------------------------------------------
     def step(self) -> None:
+        self._step(None, self.per_bucket)
+
+    def _step(self, wait, per_bucket: bool) -> None:
+        """The step's call order.  ``wait(k)``, if given, is called before the
+        first call that reads the gradient replicas of bucket k (ZeRO-3: unit
+        k) and orders the step's stream after their arrival."""
         s = self._s()
         L, C = self.L, self._call
+        ready = wait if wait is not None else (lambda k: None)
         if self.stage == 3:
             U = len(self.units)
             for u in range(U):                                   # forward
@@ -189,6 +196,7 @@ class ZeroStep:
                 C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
                 if self.transient_hook:
                     self.transient_hook("bwd", u, self.transient_rows)
+                ready(u)
                 if self.fused:
                     C("fused_step", B.zero_fused_step, L, u, self.hp, self.grad_rows, self.master_rows,
                       self.m_rows, self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
@@ -205,18 +213,22 @@ class ZeroStep:
                   self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
             return
         if self.fused:
-            if self.per_bucket:
+            if per_bucket:
                 for b in reversed(range(self.n_buckets)):
+                    ready(b)
                     C("fused_step", B.zero_fused_step, L, b, self.hp, self.grad_rows, self.master_rows,
                       self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
                       self.workspace, s)
             else:
+                for b in reversed(range(self.n_buckets)):
+                    ready(b)
                 C("fused_step", B.zero_fused_step, L, -1, self.hp, self.grad_rows, self.master_rows,
                   self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
                   self.workspace, s)
             C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
         else:
             for b in reversed(range(self.n_buckets)):
+                ready(b)
                 C("reduce_scatter", B.zero_reduce_scatter, L, b, self.grad_rows, self.gshard_rows, self.state,
                   self.workspace, s)
             C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
@@ -349,6 +361,51 @@ class ZeroStep:
         return g
 
     # -- host input ----------------------------------------------------------------------
+    def step_from_host(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
+        """One step whose N_d gradient replicas come from pinned host memory.
+
+        Each bucket's range (ZeRO-3: each unit's) is copied on two copy
+        streams in the order the step consumes them, and each reduce-scatter
+        or fused update waits only for its own range.  So later buckets cross
+        the host link while earlier ones are reduced.  This is the bucketed
+        overlap of "ZeRO: Memory Optimizations Toward Training Trillion
+        Parameter Models" reading notes §4.1-§4.2 (a bucket's reduce-scatter
+        starts as soon as backward has filled it, while the next is being
+        produced), with the host link standing in for backward.  Fused steps
+        run per bucket here.
+        The result is identical to ``upload_grads(host)`` then ``step()``."""
+        assert tuple(host.shape) == tuple(self.grads.shape) and host.dtype == self.grads.dtype
+        assert host.is_pinned(), "asynchronous host copies need pinned memory"
+        if getattr(self, "_copy_streams", None) is None:
+            self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
+        cur = self._s()
+        for cs in self._copy_streams:           # the previous step has finished reading the replicas
+            cs.wait_stream(cur)
+        if self.stage == 3:
+            order = [(u, self.units[u].offset, self.units[u].offset + self.units[u].padded)
+                     for u in reversed(range(len(self.units)))]
+        else:
+            order = [(b,) + tuple(B.zero_layout_bucket(self.L, b)) for b in reversed(range(self.n_buckets))]
+        events, i = {}, 0
+        for k, lo, hi in order:
+            for r in range(self.n_d):
+                for off in range(lo, hi, chunk_elems):
+                    end = min(hi, off + chunk_elems)
+                    with torch.cuda.stream(self._copy_streams[i % 2]):
+                        self.grads[r, off:end].copy_(host[r, off:end], non_blocking=True)
+                    i += 1
+            events[k] = []
+            for cs in self._copy_streams:
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                events[k].append(ev)
+
+        def wait(k):
+            for ev in events[k]:
+                cur.wait_event(ev)
+
+        self._step(wait, True)
+
     def upload_grads(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
         """Copy the N_d gradient replicas from (pinned) host memory, in chunks
         alternating over two copy streams (faster than one large copy on this
