@@ -97,6 +97,9 @@ def test_workload_layouts_match_oracle(name):
     (([5], None, 2, 1, 0, 48, 0), B.ZERO_ERR_INVALID),          # bucket not a multiple of 32
     (([5], None, 2, 1, 0, 0, 7), B.ZERO_ERR_INVALID),           # dtype
     (([0, 5], None, 2, 1, 0, 0, 0), B.ZERO_ERR_INVALID),        # empty tensor
+    (([5, 6], [0, (1 << 31) - 1], 2, 3, 0, 0, 0), B.ZERO_ERR_INVALID),   # unit id >= tensor count
+    (([1 << 62, 1 << 62], None, 2, 1, 0, 0, 0), B.ZERO_ERR_INVALID),   # Psi would overflow int64
+    (([5], None, 2, 1, 256 << 40, 0, 0), B.ZERO_ERR_INVALID),          # pad quantum above 2^34
 ])
 def test_layout_init_rejects(args, status):
     with pytest.raises(B.ZeroError) as e:
@@ -154,3 +157,21 @@ def test_layout_rejects_psi_pad_at_the_vector_counter_limit():
     assert e.value.status == B.ZERO_ERR_INVALID
     L = B.zero_layout_init([(1 << 34) - 1024], None, 1, 2, 0, 0, B.ZERO_BF16)
     assert B.zero_layout_query(L).psi_pad == (1 << 34) - 1024
+
+
+def test_bucket_larger_than_buffer_is_one_bucket():
+    L = B.zero_layout_init([1000, 24], None, 2, 1, 0, (1 << 62) - 32 * 3, B.ZERO_BF16)
+    info = B.zero_layout_query(L)
+    assert info.n_buckets == 1 and B.zero_layout_bucket(L, 0) == (0, info.psi_pad)
+
+
+def test_binding_refuses_pointer_lists_of_the_wrong_length():
+    # the library reads exactly N_d pointers; a shorter host list would be read past its end
+    L = B.zero_layout_init([1000, 24], None, 4, 2, 0, 0, B.ZERO_BF16)
+    for xs in ([FAKE], [FAKE] * 5):
+        with pytest.raises(B.ZeroError) as e:
+            B.zero_reduce_scatter(L, 0, xs, [FAKE] * 4, FAKE, FAKE, 0)
+        assert e.value.status == B.ZERO_ERR_INVALID
+    with pytest.raises(B.ZeroError) as e:      # NULL array: rejected by the library itself
+        B.zero_allgather_params(L, None, [FAKE] * 4, 0)
+    assert e.value.status == B.ZERO_ERR_INVALID

@@ -109,3 +109,26 @@ def test_reshard_continues_like_the_oracle(tmp_path, dst):
     else:
         for r in range(dst["n_d"]):
             assert np.array_equal(_u16(b.params[r]), zd.params16[r])
+
+
+def test_damaged_checkpoints_are_refused(tmp_path):
+    import json
+    import os
+    c = Case(NUMELS, 4, 2, FMT_BF16)
+    L = c.layout()
+    a = _engine(c)
+    a.load_master(torch.from_numpy(c.master0(L)))
+    _steps(a, c, L, 1, 1)
+    a.save_checkpoint(str(tmp_path))
+    fn = os.path.join(str(tmp_path), "rank002.bin")
+    with open(fn, "r+b") as f:                      # a truncated rank file
+        f.truncate(os.path.getsize(fn) - 4)
+    with pytest.raises(ValueError, match="rank002.bin"):
+        _engine(c).load_checkpoint(str(tmp_path))
+    a.save_checkpoint(str(tmp_path))
+    meta_fn = os.path.join(str(tmp_path), "meta.json")
+    meta = json.load(open(meta_fn))
+    meta["shard_len"] += 128                        # metadata that contradicts its own layout
+    json.dump(meta, open(meta_fn, "w"))
+    with pytest.raises(ValueError, match="shard_len"):
+        _engine(c).load_checkpoint(str(tmp_path))

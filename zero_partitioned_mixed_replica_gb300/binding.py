@@ -145,7 +145,14 @@ def _addr(x) -> int:
     return int(x.data_ptr())
 
 
-def _ptrs(xs: Sequence) -> ctypes.Array:
+def _ptrs(xs: Optional[Sequence], L: "Layout"):
+    """Host array of one device pointer per rank.  The library reads exactly
+    N_d entries, so a list of another length is refused here (a shorter one
+    would be read past its end); None passes NULL, which the library rejects."""
+    if xs is None:
+        return None
+    if len(xs) != L.n_d:
+        raise ZeroError(ZERO_ERR_INVALID, "expected %d pointers (one per rank), got %d" % (L.n_d, len(xs)))
     return (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
 
 
@@ -161,8 +168,9 @@ def _stream(s) -> int:
 class Layout:
     """Owns a ``zero_layout*``; destroyed with the object."""
 
-    def __init__(self, handle: int):
+    def __init__(self, handle: int, n_d: int):
         self.handle = ctypes.c_void_p(handle)
+        self.n_d = n_d
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None
@@ -182,7 +190,7 @@ def zero_layout_init(numels: Sequence[int], unit_of_tensor: Optional[Sequence[in
     out = ctypes.c_void_p()
     _check(lib().zero_layout_init(arr, n, units, n_d, stage, pad_multiple, bucket_elems, dtype,
                                   ctypes.byref(out)))
-    return Layout(out.value)
+    return Layout(out.value, n_d)
 
 
 def zero_layout_query(L: Layout) -> zero_layout_info:
@@ -223,7 +231,7 @@ def zero_state_init(st, beta1: float, beta2: float, loss_scale: float = 1.0, dyn
 
 def zero_reduce_scatter(L: Layout, bucket_or_unit: int, grad_replicas, grad_shards, st, workspace,
                         stream=None) -> None:
-    _check(lib().zero_reduce_scatter(L, bucket_or_unit, _ptrs(grad_replicas), _ptrs(grad_shards), _addr(st),
+    _check(lib().zero_reduce_scatter(L, bucket_or_unit, _ptrs(grad_replicas, L), _ptrs(grad_shards, L), _addr(st),
                                      _addr(workspace), _stream(stream)))
 
 
@@ -237,31 +245,31 @@ def _hp(lr, eps, weight_decay) -> zero_adamw_hp:
 
 def zero_adamw_shard_step(L: Layout, hp: zero_adamw_hp, master, m, v, grad_shards, st, param16_out,
                           out_kind: int, stream=None) -> None:
-    _check(lib().zero_adamw_shard_step(L, ctypes.byref(hp), _ptrs(master), _ptrs(m), _ptrs(v),
-                                       _ptrs(grad_shards), _addr(st), _ptrs(param16_out), out_kind,
+    _check(lib().zero_adamw_shard_step(L, ctypes.byref(hp), _ptrs(master, L), _ptrs(m, L), _ptrs(v, L),
+                                       _ptrs(grad_shards, L), _addr(st), _ptrs(param16_out, L), out_kind,
                                        _stream(stream)))
 
 
 def zero_allgather_params(L: Layout, param16_shards, param16_full, stream=None) -> None:
-    _check(lib().zero_allgather_params(L, _ptrs(param16_shards), _ptrs(param16_full), _stream(stream)))
+    _check(lib().zero_allgather_params(L, _ptrs(param16_shards, L), _ptrs(param16_full, L), _stream(stream)))
 
 
 def zero_stage3_gather_layer(L: Layout, unit: int, param16_shards, transient, stream=None) -> None:
-    _check(lib().zero_stage3_gather_layer(L, unit, _ptrs(param16_shards), _ptrs(transient), _stream(stream)))
+    _check(lib().zero_stage3_gather_layer(L, unit, _ptrs(param16_shards, L), _ptrs(transient, L), _stream(stream)))
 
 
 def zero_fused_step(L: Layout, bucket_or_unit: int, hp: zero_adamw_hp, grad_replicas, master, m, v, st,
                     param16_out, out_kind: int, workspace, stream=None) -> None:
-    _check(lib().zero_fused_step(L, bucket_or_unit, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master),
-                                 _ptrs(m), _ptrs(v), _addr(st), _ptrs(param16_out), out_kind,
+    _check(lib().zero_fused_step(L, bucket_or_unit, ctypes.byref(hp), _ptrs(grad_replicas, L), _ptrs(master, L),
+                                 _ptrs(m, L), _ptrs(v, L), _addr(st), _ptrs(param16_out, L), out_kind,
                                  _addr(workspace), _stream(stream)))
 
 
 def zero_fused_step_noalloc(L: Layout, hp: zero_adamw_hp, grad_replicas, master, m, v, st, param16_out,
                             out_kind: int, stream=None) -> None:
     """Whole fused step without a caller workspace (see include/zero.h)."""
-    _check(lib().zero_fused_step_noalloc(L, ctypes.byref(hp), _ptrs(grad_replicas), _ptrs(master), _ptrs(m),
-                                         _ptrs(v), _addr(st), _ptrs(param16_out), out_kind, _stream(stream)))
+    _check(lib().zero_fused_step_noalloc(L, ctypes.byref(hp), _ptrs(grad_replicas, L), _ptrs(master, L), _ptrs(m, L),
+                                         _ptrs(v, L), _addr(st), _ptrs(param16_out, L), out_kind, _stream(stream)))
 
 
 def zero_reshard_plan(src: Layout, dst: Layout):
@@ -274,19 +282,19 @@ def zero_reshard_plan(src: Layout, dst: Layout):
 
 
 def zero_accumulate_grads(L: Layout, micro: int, grad_replicas, acc_replicas, stream=None) -> None:
-    _check(lib().zero_accumulate_grads(L, micro, _ptrs(grad_replicas), _ptrs(acc_replicas), _stream(stream)))
+    _check(lib().zero_accumulate_grads(L, micro, _ptrs(grad_replicas, L), _ptrs(acc_replicas, L), _stream(stream)))
 
 
 def zero_reduce_scatter_accumulated(L: Layout, bucket: int, acc_replicas, grad_shards, n_micro: int, st, workspace,
                                     stream=None) -> None:
-    _check(lib().zero_reduce_scatter_accumulated(L, bucket, _ptrs(acc_replicas), _ptrs(grad_shards), n_micro,
+    _check(lib().zero_reduce_scatter_accumulated(L, bucket, _ptrs(acc_replicas, L), _ptrs(grad_shards, L), n_micro,
                                                  _addr(st), _addr(workspace), _stream(stream)))
 
 
 def zero_reduce_scatter_micro(L: Layout, bucket_or_unit: int, micro: int, n_micro: int, grad_replicas, acc_shards,
                               st, workspace, stream=None) -> None:
-    _check(lib().zero_reduce_scatter_micro(L, bucket_or_unit, micro, n_micro, _ptrs(grad_replicas),
-                                           _ptrs(acc_shards), _addr(st), _addr(workspace), _stream(stream)))
+    _check(lib().zero_reduce_scatter_micro(L, bucket_or_unit, micro, n_micro, _ptrs(grad_replicas, L),
+                                           _ptrs(acc_shards, L), _addr(st), _addr(workspace), _stream(stream)))
 
 
 def zero_set_max_ctas(n: int) -> int:

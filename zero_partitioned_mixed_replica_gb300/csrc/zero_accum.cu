@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) rs_acc_kernel(const __grid_constant_
     const uint32_t gw = (blockIdx.x * kThreads + threadIdx.x) >> 5;
     const uint32_t nw = (gridDim.x * kThreads) >> 5;
     const int nd = ND > 0 ? ND : a.nd;
-    const float D = __double2float_rn(__dmul_rn((double)(nd * a.n_micro), (double)a.st->loss_scale));
+    const float D = __double2float_rn(__dmul_rn(__dmul_rn((double)nd, (double)a.n_micro), (double)a.st->loss_scale));
     bool bad = false;
     for (uint32_t base = a.seg.v_begin + gw * 32u; base < a.seg.v_end; base += nw * 32u) {
         const uint32_t v = base + lane;

@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::bar_off);
     __shared__ AdamConsts sk;
     __shared__ int s_apply, s_abort;
+    __shared__ uint32_t s_stop;
     const int tid = threadIdx.x;
     if (tid == 0) {
         const zero_step_state* st = a.st;
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
         const bool ok = mbar_wait_bounded(&full[slot], (kk / STAGES) & 1u);
         if (!ok) {
             s_abort = 1;
+            s_stop = kk;  // every thread that gives up writes the same tile index
             atomicOr(&a.st->error, ZERO_DEVERR_WAIT_TIMEOUT);
         }
         uint32_t r, len;
@@ -147,7 +149,16 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all<0>();
+    if (tid == 0) {
+        if (s_abort) {
+            // After a timed-out wait on tile s_stop, let the loads still in
+            // flight (tiles s_stop .. s_stop + STAGES - 1) land, each wait
+            // bounded again, before the CTA gives up its shared memory.
+            const uint32_t k0 = s_stop, k1 = min(count, k0 + (uint32_t)STAGES);
+            for (uint32_t j = k0; j < k1; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u);
+        }
+        bulk_wait_all<0>();
+    }
 }
 
 // Four CTAs of 256 threads per SM (64 registers, no spills): the shard-output

@@ -346,7 +346,7 @@ __device__ __forceinline__ void bulk_wait_all() {
 // ----------------------------------------------------------------------------
 // Kernel arguments (passed by value as __grid_constant__ parameters).
 // Vector indices count 8-element vectors of the flat buffer (32-bit: the
-// layout rejects Psi_pad >= 2^35).
+// layout rejects Psi_pad >= 2^34).
 // ----------------------------------------------------------------------------
 struct SegArgs {
     uint32_t v_begin, v_end;  // flat vector range processed by this launch

@@ -36,6 +36,10 @@ int64_t partials_count(const zero_layout* L) { return L->psi_pad / kGroup; }
 
 static int64_t round_up(int64_t x, int64_t m) { return ((x + m - 1) / m) * m; }
 
+// Largest Psi and pad quantum accepted (the kernels' vector counters need
+// Psi_pad / 8 < 2^31 in any case); it keeps every size sum inside int64.
+static constexpr int64_t kMaxElems = (int64_t)1 << 34;
+
 int64_t workspace_bytes(const zero_layout* L) {
     int64_t p = round_up(partials_count(L) * (int64_t)sizeof(float), 256);
     return p + round_up((int64_t)kNormBlocks * (int64_t)sizeof(double), 256);
@@ -69,8 +73,8 @@ extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tenso
     if (dtype != ZERO_BF16 && dtype != ZERO_FP16) return fail(ZERO_ERR_INVALID, "layout: dtype must be bf16 or fp16");
     const int64_t quantum = (int64_t)n_d * 128;
     int64_t q = pad_multiple > 0 ? pad_multiple : quantum;
-    if (pad_multiple < 0 || q % quantum != 0)
-        return fail(ZERO_ERR_INVALID, "layout: pad_multiple must be 0 or a positive multiple of n_d*128");
+    if (pad_multiple < 0 || q % quantum != 0 || q > kMaxElems)
+        return fail(ZERO_ERR_INVALID, "layout: pad_multiple must be 0 or a positive multiple of n_d*128 (<= 2^34)");
     if (bucket_elems > 0 && bucket_elems % kGroup != 0)
         return fail(ZERO_ERR_INVALID, "layout: bucket_elems must be <= 0 or a multiple of 32");
     if (stage == 3 && !unit_of_tensor) return fail(ZERO_ERR_INVALID, "layout: stage 3 needs unit_of_tensor");
@@ -90,6 +94,10 @@ extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tenso
             delete L;
             return fail(ZERO_ERR_INVALID, "layout: every tensor needs numel > 0");
         }
+        if (numels[t] > kMaxElems - psi) {  // also keeps every later sum and rounding inside int64
+            delete L;
+            return fail(ZERO_ERR_INVALID, "layout: Psi too large (> 2^34 elements)");
+        }
         psi += numels[t];
     }
     L->psi = psi;
@@ -97,9 +105,10 @@ extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tenso
     if (stage == 3) {
         int32_t n_units = 0;
         for (int32_t t = 0; t < n_tensors; ++t) {
-            if (unit_of_tensor[t] < 0) {
+            // no unit may be empty, so every id is below the tensor count
+            if (unit_of_tensor[t] < 0 || unit_of_tensor[t] >= n_tensors) {
                 delete L;
-                return fail(ZERO_ERR_INVALID, "layout: negative unit id");
+                return fail(ZERO_ERR_INVALID, "layout: unit ids must lie in 0..n_tensors-1");
             }
             n_units = std::max(n_units, unit_of_tensor[t] + 1);
         }
@@ -111,14 +120,14 @@ extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tenso
                 return fail(ZERO_ERR_INVALID, "layout: unit ids must cover 0..U-1 with no empty unit");
             }
         }
+        std::vector<std::vector<int32_t>> members(n_units);  // tensors of each unit, in declaration order
+        for (int32_t t = 0; t < n_tensors; ++t) members[unit_of_tensor[t]].push_back(t);
         int64_t off = 0, base = 0;
         for (int32_t u = 0; u < n_units; ++u) {
             int64_t r = 0;
-            for (int32_t t = 0; t < n_tensors; ++t) {
-                if (unit_of_tensor[t] == u) {
-                    L->tensor_offset[t] = off + r;
-                    r += numels[t];
-                }
+            for (int32_t t : members[u]) {
+                L->tensor_offset[t] = off + r;
+                r += numels[t];
             }
             zero_segment s;
             s.offset = off;
@@ -149,7 +158,7 @@ extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tenso
         L->segs.push_back(s);
         L->psi_pad = s.padded;
         L->shard_len = s.shard;
-        if (bucket_elems <= 0) {
+        if (bucket_elems <= 0 || bucket_elems >= L->psi_pad) {
             L->buckets.emplace_back(0, L->psi_pad);
             L->bucket_seg.push_back(0);
         } else {

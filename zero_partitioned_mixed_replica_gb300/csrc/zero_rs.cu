@@ -15,7 +15,7 @@ namespace zk {
 
 // D = binary32(N_d * n_micro * loss_scale): the exact product rounded once.
 __device__ __forceinline__ float rs_divisor(int nd, int n_micro, float loss_scale) {
-    return __double2float_rn(__dmul_rn((double)(nd * n_micro), (double)loss_scale));
+    return __double2float_rn(__dmul_rn(__dmul_rn((double)nd, (double)n_micro), (double)loss_scale));
 }
 
 // Combine the rank-order sum s with the accumulator for the reduce-scatter

@@ -473,8 +473,17 @@ class ZeroStep:
             raise ValueError("checkpoint dtype differs")
         plan = B.zero_reshard_plan(src, self.L)
         S0, S = meta["shard_len"], self.info.shard_len
-        files = [np.memmap(os.path.join(path, "rank%03d.bin" % r), dtype=np.uint8, mode="r")
-                 for r in range(meta["n_d"])]
+        if B.zero_layout_query(src).shard_len != S0:
+            raise ValueError("checkpoint shard_len %d does not match its own layout" % S0)
+        st = bytes.fromhex(meta["state"])
+        if len(st) != self.state.numel():
+            raise ValueError("checkpoint step state has %d bytes, expected %d" % (len(st), self.state.numel()))
+        files = []
+        for r in range(meta["n_d"]):
+            fn = os.path.join(path, "rank%03d.bin" % r)
+            if os.path.getsize(fn) != 14 * S0:      # fp32 master, m, v + 16-bit parameters per element
+                raise ValueError("%s holds %d bytes, expected %d" % (fn, os.path.getsize(fn), 14 * S0))
+            files.append(np.memmap(fn, dtype=np.uint8, mode="r"))
         views = []
         for mm in files:
             f32 = mm[:12 * S0].view(np.float32)
@@ -497,7 +506,6 @@ class ZeroStep:
                 self.m[r].copy_(torch.from_numpy(host[1]))
                 self.v[r].copy_(torch.from_numpy(host[2]))
                 p16_rows[r].view(torch.int16).copy_(torch.from_numpy(host[3].view(np.int16)))
-        st = bytes.fromhex(meta["state"])
         self.state.copy_(torch.frombuffer(bytearray(st), dtype=torch.uint8))
         if self.stage != 3:
             if self.shard16 is None:
