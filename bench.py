@@ -139,6 +139,24 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def host_link_gbs(host: torch.Tensor, dev_buf: torch.Tensor, stream, nbytes: int = 2 << 30) -> float:
+    """Host-to-device rate of this box's link, measured just before the e2e
+    leg: the best of three 2 GB pinned copies into the gradient buffer (whose
+    contents the e2e steps overwrite anyway)."""
+    n = min(host.numel(), nbytes // host.element_size())
+    src, dst = host.view(-1)[:n], dev_buf.view(-1)[:n]
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+    return n * host.element_size() / (best / 1e3) / 1e9
+
+
 def max_over_ranks(value: float, world: int) -> float:
     """The slowest rank's time (gloo all-reduce MAX on the host); the value
     itself on a single rank."""
@@ -322,6 +340,7 @@ def gpu_run(args, w, rank, world, local_rank):
             host_grads = torch.empty(tuple(eng.grads.shape), dtype=eng.grads.dtype, pin_memory=True)
             host_grads.copy_(eng.grads)
             host_state = torch.empty(96, dtype=torch.uint8).pin_memory()
+            link_gbs = host_link_gbs(host_grads, eng.grads, stream)
             torch.cuda.synchronize(dev)
             if world > 1:
                 dist.barrier()
@@ -340,7 +359,9 @@ def gpu_run(args, w, rank, world, local_rank):
             ems = max_over_ranks(a.elapsed_time(b), world)
             e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
                    "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()) * args.micro,
-                   "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps}
+                   "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps,
+                   "host_link_gbs": link_gbs,
+                   "h2d_floor_ms": int(eng.grads.numel() * eng.grads.element_size()) * args.micro / link_gbs / 1e6}
             del host_grads
         except RuntimeError as ex:
             e2e = {"value": None, "unit": "params/s", "error": str(ex)[:200]}
