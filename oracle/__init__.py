@@ -16,5 +16,10 @@ Pins (tests marked ``not gpu``): the pages' memory tables and worked values,
 the exact communication-volume forms, brute-force layout checks, library
 round-to-nearest-even casts, exact rational sums, the closed form of AdamW
 under a constant gradient, ``torch.optim.AdamW`` at N_d = 1, the closed-form
-norm of a constant gradient, the fp16 overflow skip, and ZeRO-k == DDP.
+norm of a constant gradient, the fp16 overflow skip, and ZeRO-k == DDP; for
+gradient accumulation, exact rational bounds for both summation orders and
+M = 1 == the plain step; the sampled form (``SampledElements``,
+``FullSumsq``) reproduces the whole-buffer simulation bit for bit; and
+planted mistakes (bias correction, decay, betas, eps, coupled decay, a dropped
+rank, the divisor) each fail one of the pins.
 """
