@@ -143,6 +143,7 @@ def host_link_gbs(host: torch.Tensor, dev_buf: torch.Tensor, stream, nbytes: int
     """Host-to-device rate of this box's link, measured just before the e2e
     leg: the best of three 2 GB pinned copies into the gradient buffer (whose
     contents the e2e steps overwrite anyway)."""
+    import torch
     n = min(host.numel(), nbytes // host.element_size())
     src, dst = host.view(-1)[:n], dev_buf.view(-1)[:n]
     best = float("inf")
@@ -341,12 +342,8 @@ def gpu_run(args, w, rank, world, local_rank):
             host_grads.copy_(eng.grads)
             host_state = torch.empty(96, dtype=torch.uint8).pin_memory()
             link_gbs = host_link_gbs(host_grads, eng.grads, stream)
-            torch.cuda.synchronize(dev)
-            if world > 1:
-                dist.barrier()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.e2e_steps):
+
+            def e2e_step():
                 if args.micro == 1:
                     eng.step_from_host(host_grads)     # per-bucket copies overlap the reduce-scatter
                 else:
@@ -354,13 +351,26 @@ def gpu_run(args, w, rank, world, local_rank):
                         eng.upload_grads(host_grads)
                         eng.micro_step(mb)
                 host_state.copy_(eng.state, non_blocking=True)
+
+            # Untimed warm-up, as for the device-resident steps: the first
+            # whole-buffer passes over a freshly pinned buffer cross the host
+            # link at 90-140 GB/s before settling at the link rate.
+            for _ in range(max(3, args.warmup)):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
             b.record(stream)
             torch.cuda.synchronize(dev)
             ems = max_over_ranks(a.elapsed_time(b), world)
             e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
                    "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()) * args.micro,
                    "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps,
-                   "host_link_gbs": link_gbs,
+                   "warmup_steps": max(3, args.warmup), "host_link_gbs": link_gbs,
                    "h2d_floor_ms": int(eng.grads.numel() * eng.grads.element_size()) * args.micro / link_gbs / 1e6}
             del host_grads
         except RuntimeError as ex:

@@ -40,24 +40,40 @@ __global__ void state_init_kernel(zero_step_state* st, double beta1, double beta
 }
 
 // Pass 1: block b sums a fixed contiguous range of the partials (fixed
-// thread-strided assignment).  Each thread accumulates in binary32 with an
-// error-free TwoSum carry (hi + lo holds the sum to ~2^-48 relative; binary64
-// arithmetic is slow on this part), then the block combines the threads'
-// hi + lo in binary64 through a fixed pairwise tree.
+// thread-strided assignment of 16-byte vectors).  Each thread keeps four
+// binary32 chains, one per vector lane, each with an error-free TwoSum carry
+// (hi + lo holds a chain's sum to ~2^-48 relative; binary64 arithmetic is
+// slow on this part), and merges them in lane order; the block then combines
+// the threads' hi + lo in binary64 through a fixed pairwise tree.  The range
+// length is a multiple of 4 partials (Psi_pad is a multiple of 128), so every
+// vector is whole and 16-byte aligned.
 __global__ void __launch_bounds__(256) norm_blocks_kernel(const float* __restrict__ partials, uint32_t count,
                                                           double* __restrict__ block_sums) {
-    const uint32_t chunk = (count + gridDim.x - 1) / gridDim.x;
-    const uint32_t b0 = blockIdx.x * chunk;
+    const uint32_t chunk = ((count + gridDim.x - 1) / gridDim.x + 3u) & ~3u;
+    const uint32_t b0 = min(count, blockIdx.x * chunk);
     const uint32_t b1 = min(count, b0 + chunk);
-    float hi = 0.0f, lo = 0.0f;
-    for (uint32_t i = b0 + threadIdx.x; i < b1; i += blockDim.x) {
+    const float4* p4 = reinterpret_cast<const float4*>(partials);
+    float hi[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lo[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (uint32_t i = b0 / 4 + threadIdx.x; i < b1 / 4; i += blockDim.x) {
+        const float4 x = __ldcs(p4 + i);
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float s, e;
+            two_sum(hi[c], xs[c], s, e);
+            hi[c] = s;
+            lo[c] = __fadd_rn(lo[c], e);
+        }
+    }
+#pragma unroll
+    for (int c = 1; c < 4; ++c) {
         float s, e;
-        two_sum(hi, partials[i], s, e);
-        hi = s;
-        lo = __fadd_rn(lo, e);
+        two_sum(hi[0], hi[c], s, e);
+        hi[0] = s;
+        lo[0] = __fadd_rn(__fadd_rn(lo[0], lo[c]), e);
     }
     __shared__ double sh[256];
-    sh[threadIdx.x] = __dadd_rn((double)hi, (double)lo);
+    sh[threadIdx.x] = __dadd_rn((double)hi[0], (double)lo[0]);
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
         if ((int)threadIdx.x < w) sh[threadIdx.x] = __dadd_rn(sh[threadIdx.x], sh[threadIdx.x + w]);
