@@ -277,9 +277,30 @@ static zero_status_t launch_adamw(const zk::AdamArgs& a, int out_kind, cudaStrea
     return launch_adamw_tma<ND, F, ZERO_OUT_SHARDS, 2048, 4, 2>(a, s);
 }
 
+// Resident CTAs per SM for the fused step.  All four that fit are not always
+// best: with many replica streams in flight per thread, fewer CTAs keep the
+// DRAM pages busier.  GB300, ms per step with 4 / 3 / 2 CTAs per SM:
+//   full replicas: N_d=2 (350M) 1.861 / 1.772 / 2.097; N_d=4 2.333 / 2.229 /
+//   2.436; N_d=8 (124M) 1.165 / 1.162 / 1.089, (350M) 3.267 / 3.274 / 3.067;
+//   N_d=16 5.056 / 4.934 / 5.556; N_d=64 15.95 / 15.82 / 15.71;
+//   shard output (ZeRO-3 units): N_d=2 (7B block) 1.381 / 1.387 / 1.571;
+//   N_d=8 (350M) 4.840 / 4.762 / 5.031.
+// Launches too short to give every thread ~32 vectors at the reduced grid
+// keep all four (5M-element buckets, N_d=8: 1.282 / 1.308 / 1.347).
+static int64_t fused_ctas_cap(int nd, int out_kind, int64_t nvec) {
+    int k = 4;
+    if (nd > 1 && out_kind == ZERO_OUT_FULL_REPLICAS) k = nd == 8 ? 2 : 3;
+    if (out_kind == ZERO_OUT_SHARDS && nd == 8) k = 3;
+    const int64_t sms = sm_count() > 0 ? sm_count() : 1;
+    if (nvec < 32 * (int64_t)k * sms * zk::kThreads) k = 4;
+    return (int64_t)k * sms;
+}
+
 template <int ND, class F>
 static zero_status_t launch_fused(const zk::FusedArgs& a, int64_t nvec, int out_kind, cudaStream_t s) {
-    const int64_t work = (nvec + zk::kThreads - 1) / zk::kThreads;
+    const int64_t need = (nvec + zk::kThreads - 1) / zk::kThreads;
+    const int64_t cap = fused_ctas_cap(a.nd, out_kind, nvec);
+    const int64_t work = need < cap ? need : cap;
     if (out_kind == ZERO_OUT_FULL_REPLICAS) {
         auto kern = zk::fused_kernel<ND, F, ZERO_OUT_FULL_REPLICAS>;
         kern<<<persistent_grid(kern, work), zk::kThreads, 0, s>>>(a);
