@@ -139,23 +139,24 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
-def host_link_gbs(host: torch.Tensor, dev_buf: torch.Tensor, stream, nbytes: int = 2 << 30) -> float:
+def host_link_gbs(host: torch.Tensor, dev_buf: torch.Tensor, stream) -> float:
     """Host-to-device rate of this box's link, measured just before the e2e
-    leg: the best of three 2 GB pinned copies into the gradient buffer (whose
-    contents the e2e steps overwrite anyway)."""
+    leg: the better of two pinned copies of the whole gradient buffer into
+    its device twin (whose contents the e2e steps overwrite anyway).  The
+    link is shared with other tenants of the host, so it is taken at the
+    size and moment of the e2e leg."""
     import torch
-    n = min(host.numel(), nbytes // host.element_size())
-    src, dst = host.view(-1)[:n], dev_buf.view(-1)[:n]
+    src, dst = host.view(-1), dev_buf.view(-1)
     best = float("inf")
     with torch.cuda.stream(stream):
-        for _ in range(3):
+        for _ in range(2):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             dst.copy_(src, non_blocking=True)
             b.record(stream)
             b.synchronize()
             best = min(best, a.elapsed_time(b))
-    return n * host.element_size() / (best / 1e3) / 1e9
+    return src.numel() * host.element_size() / (best / 1e3) / 1e9
 
 
 def max_over_ranks(value: float, world: int) -> float:
