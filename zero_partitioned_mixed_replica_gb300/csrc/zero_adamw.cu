@@ -165,6 +165,47 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
 // variant otherwise takes 68 registers and three CTAs, and at N_d = 2 its
 // ~30 B/param leave it bound by latency (7B ZeRO-3 unit update 0.977 ->
 // 0.941 ms).  Five CTAs per SM force spills.
+// The same update with plain 32-byte loads and stores, 8 elements per thread
+// over the rank-major shard space.  With few bytes per element (the 16-bit
+// shard output of ZeRO-3) the TMA pipeline's per-tile barriers dominate and
+// this form is faster; results are identical (same per-element update).
+template <int ND, class F, int OUT>
+__global__ void __launch_bounds__(kThreads, 4) adamw_ldg_kernel(const __grid_constant__ AdamArgs a) {
+    __shared__ AdamConsts sk;
+    __shared__ int s_apply;
+    if (threadIdx.x == 0) {
+        const zero_step_state* st = a.st;
+        s_apply = st->apply;
+        sk = make_consts(st->beta1, st->beta2, st->beta1_pow, st->beta2_pow, a.lr, a.eps, a.wd, st->clip_coef);
+    }
+    __syncthreads();
+    if (!s_apply) return;  // overflow: the step is skipped
+    const AdamConsts k = sk;
+    const int nd = ND > 0 ? ND : a.nd;
+    for (uint32_t v = blockIdx.x * kThreads + threadIdx.x; v < a.total_v; v += gridDim.x * kThreads) {
+        const uint32_t r = v / a.shard_v;
+        const uint32_t j = v - r * a.shard_v;
+        const size_t o = (size_t)j * kVec;
+        float g[8], p[8], m[8], w[8];
+        ld8(a.gshard[r] + o, g);
+        ld8(a.master[r] + o, p);
+        ld8(a.m[r] + o, m);
+        ld8(a.v[r] + o, w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) adamw1(p[e], m[e], w[e], g[e], k);
+        st8(a.master[r] + o, p);
+        st8(a.m[r] + o, m);
+        st8(a.v[r] + o, w);
+        const uint4 h = pack8<F>(p);
+        if constexpr (OUT == ZERO_OUT_FULL_REPLICAS) {
+            const size_t fo = (size_t)v * kVec;  // ZeRO-1/2: rank-major shard order is flat order
+            for (int q = 0; q < nd; ++q) st_stream(a.out[q] + fo, h);
+        } else {
+            st_stream(a.out[r] + o, h);
+        }
+    }
+}
+
 template <int ND, class F, int OUT>
 __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constant__ FusedArgs a) {
     __shared__ AdamConsts sk;
@@ -258,8 +299,9 @@ static zero_status_t launch_adamw_tma(const zk::AdamArgs& a, cudaStream_t s) {
     const int64_t tiles = ((S + TE - 1) / TE) * a.nd;
     // With few bytes per element (16-bit shard output, or at most 4 replicas)
     // the update is bound by instruction latency, and 16 warps per SM beat 8
-    // (7B ZeRO-3 shard update 50.2 -> 43.9 ms); with 8 replicas it is bound by
-    // bandwidth and 8 warps are faster (10.99 vs 11.38 ms at 1.5B).
+    // (7B ZeRO-3 shard update 50.2 -> 43.9 ms, before shard outputs moved to
+    // the LDG form); with 8 replicas it is bound by bandwidth and 8 warps are
+    // faster (10.99 vs 11.38 ms at 1.5B).
     if (OUT == ZERO_OUT_SHARDS || a.nd <= 4)
         return launch_tma(zk::adamw_tma_kernel<ND, F, OUT, TE, STAGES, OST, 512>,
                           zk::AdamTmaSmem<TE, STAGES, OST>::total, tiles, a, s, 512);
@@ -271,8 +313,28 @@ static zero_status_t launch_adamw_tma(const zk::AdamArgs& a, cudaStream_t s) {
 // memory, one CTA per SM): on GB300 this shape reaches 98% of the bandwidth a
 // plain streaming kernel gets for the 16-byte-read / 28-byte-write mix of the
 // 8-replica update.
+template <int ND, class F, int OUT>
+static zero_status_t launch_adamw_ldg(const zk::AdamArgs& a, cudaStream_t s) {
+    auto kern = zk::adamw_ldg_kernel<ND, F, OUT>;
+    const int64_t work = ((int64_t)a.total_v + zk::kThreads - 1) / zk::kThreads;
+    kern<<<persistent_grid(kern, work), zk::kThreads, 0, s>>>(a);
+    return after_launch("zero_adamw_shard_step");
+}
+
+// Which form of the update runs (GB300, ms per AdamW call, LDG / TMA): the
+// 16-bit shard output of ZeRO-3 moves 30 B per element, too few for the TMA
+// pipeline's per-tile barriers (7B block unit 0.965 / 1.204; 350M at N_d = 2,
+// 8, 64: 1.67 / 2.07-2.11); full replicas at N_d = 2 also favour LDG (350M
+// 1.815 / 1.884), while at N_d = 4..64 the TMA form is equal or faster (350M
+// N_d = 4 2.06 / 1.99, N_d = 8 2.53 / 2.49, N_d = 64 9.58 / 9.51; the 1.5B
+// block at N_d = 8 0.224 / 0.225).
 template <int ND, class F>
 static zero_status_t launch_adamw(const zk::AdamArgs& a, int out_kind, cudaStream_t s) {
+    const bool ldg = out_kind == ZERO_OUT_SHARDS || a.nd == 2;
+    if (ldg) {
+        if (out_kind == ZERO_OUT_SHARDS) return launch_adamw_ldg<ND, F, ZERO_OUT_SHARDS>(a, s);
+        return launch_adamw_ldg<ND, F, ZERO_OUT_FULL_REPLICAS>(a, s);
+    }
     if (out_kind == ZERO_OUT_FULL_REPLICAS) return launch_adamw_tma<ND, F, ZERO_OUT_FULL_REPLICAS, 2048, 4, 2>(a, s);
     return launch_adamw_tma<ND, F, ZERO_OUT_SHARDS, 2048, 4, 2>(a, s);
 }
