@@ -29,10 +29,11 @@ class Case:
     inf_step: Optional[int] = None
     inf_rank: int = 0
     seed: int = 1234
+    pad_multiple: int = 0
 
     def layout(self) -> Layout:
         return make_layout(self.numels, self.n_d, self.stage, bucket_elems=self.bucket_elems,
-                           unit_of_tensor=self.units)
+                           unit_of_tensor=self.units, pad_multiple=self.pad_multiple)
 
     def master0(self, L: Layout) -> np.ndarray:
         return synth.master_init(L.numels, L.tensor_offsets, L.psi_pad, seed=self.seed).numpy()

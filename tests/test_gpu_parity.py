@@ -34,7 +34,7 @@ def _engine(case: Case, **kw):
     from zero_partitioned_mixed_replica_gb300.engine import AdamW, ZeroStep
     return ZeroStep(case.numels, case.n_d, case.stage, case.fmt, case.bucket_elems, case.units,
                     AdamW(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay), case.max_norm,
-                    case.loss_scale, case.dynamic, case.growth_interval, **kw)
+                    case.loss_scale, case.dynamic, case.growth_interval, pad_multiple=case.pad_multiple, **kw)
 
 
 def _u16(t: torch.Tensor) -> np.ndarray:
@@ -337,3 +337,12 @@ def test_units_smaller_than_a_rank_slice():
     c = Case([3, 5000, 5, 70_000], 4, 3, FMT_FP16, units=[0, 1, 2, 3], max_norm=0.1, loss_scale=512.0,
              dynamic=True)
     run_parity(c, 2, use_gpu_clip=True)
+
+
+@pytest.mark.parametrize("stage,units", [(2, None), (3, [0, 1, 1, 2])])
+def test_user_pad_multiple(stage, units):
+    # a pad quantum of 4 N_d 128 (a DeepSpeed-style alignment knob): more padding, same results
+    c = Case([120_000, 7, 50_001, 3000], 3, stage, FMT_BF16, bucket_elems=32_768 if stage != 3 else 0,
+             units=units, max_norm=0.05, pad_multiple=4 * 3 * 128)
+    eng, zs, _ = run_parity(c, 2, use_gpu_clip=True)
+    assert eng.info.q == 4 * 3 * 128 and eng.info.psi_pad % (4 * 3 * 128) == 0

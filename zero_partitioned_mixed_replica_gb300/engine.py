@@ -52,11 +52,13 @@ class ZeroStep:
                  adamw: AdamW = AdamW(), max_norm: float = 0.0, loss_scale: float = 1.0,
                  dynamic_scale: bool = False, growth_interval: int = 2000,
                  fused: Optional[bool] = None, per_bucket: bool = True, fuse_allgather: bool = True,
-                 n_micro: int = 1, device: str = "cuda", stream: Optional[torch.cuda.Stream] = None):
+                 n_micro: int = 1, device: str = "cuda", stream: Optional[torch.cuda.Stream] = None,
+                 pad_multiple: int = 0):
         if stage not in (1, 2, 3):
             raise ValueError("ZeroStep runs ZeRO stages 1, 2 and 3")
+        self.pad_multiple = pad_multiple    # 0: N_d * 128; else a multiple of it
         self.L = B.zero_layout_init(list(numels), list(unit_of_tensor) if unit_of_tensor is not None else None,
-                                    n_d, stage, 0, bucket_elems, dtype)
+                                    n_d, stage, pad_multiple, bucket_elems, dtype)
         self.info = B.zero_layout_query(self.L)
         self.n_d, self.stage, self.dtype = n_d, stage, dtype
         self.adamw = adamw
@@ -117,7 +119,7 @@ class ZeroStep:
         padded length and shards do not depend on it, so nothing moves."""
         if self.stage == 3:
             raise ValueError("ZeRO-3 reduces per unit")
-        L = B.zero_layout_init(self.numels, None, self.n_d, self.stage, 0, bucket_elems, self.dtype)
+        L = B.zero_layout_init(self.numels, None, self.n_d, self.stage, self.pad_multiple, bucket_elems, self.dtype)
         info = B.zero_layout_query(L)
         assert info.psi_pad == self.info.psi_pad and info.shard_len == self.info.shard_len
         self.L, self.info, self.n_buckets = L, info, info.n_buckets
