@@ -223,7 +223,11 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_timing(w, sample_params: int, min_seconds: float, min_steps: int = 3, max_steps: int = 10 ** 6):
+def oracle_timing(w, sample_params: int, min_seconds: float, min_steps: int = 3, max_steps: int = 10 ** 6,
+                  warmup: int = 1):
+    """The oracle's step on a bounded sample of the workload: ``warmup``
+    untimed steps, then at least ``min_steps`` timed steps and at least
+    ``min_seconds`` of them (at most ``max_steps``)."""
     import numpy as np
     from oracle.layout import make_layout
     from oracle.step import AdamWHP, ZeroSimulation, num_threads
@@ -239,7 +243,8 @@ def oracle_timing(w, sample_params: int, min_seconds: float, min_steps: int = 3,
     zs = ZeroSimulation(L, m0, w.dtype, AdamWHP(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay),
                         max_norm=w.max_norm, loss_scale=w.loss_scale, dynamic=w.dynamic_scale,
                         growth_interval=w.growth_interval)
-    zs.step(reps)                                   # warm-up
+    for _ in range(warmup):                         # untimed warm-up steps
+        zs.step(reps)
     n, t0 = 0, time.perf_counter()
     while n < max_steps and (n < min_steps or time.perf_counter() - t0 < min_seconds):
         zs.step(reps)
@@ -555,9 +560,11 @@ def main():
         if rank != 0:
             return
         sample = args.cpu_sample or default_sample(w)
-        cb = oracle_timing(w, sample, min_seconds=max(1.0, args.cpu_seconds), min_steps=max(1, args.steps))
+        # exactly W untimed and K timed oracle steps, each on the bounded sample
+        cb = oracle_timing(w, sample, min_seconds=0.0, min_steps=max(1, args.steps), max_steps=max(1, args.steps),
+                           warmup=max(0, args.warmup))
         line = {"metric": METRIC, "value": cb["value"], "unit": "params/s", "impl": "reference",
-                "n_gpus": args.gpus, "steps": cb["steps"], "warmup": 1,
+                "n_gpus": args.gpus, "steps": cb["steps"], "warmup": max(0, args.warmup),
                 "ms_per_step": cb["s_per_step"] * 1e3 * w.psi / sample,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic", "config": workload_desc,
