@@ -69,7 +69,7 @@ enum {
     ZERO_ERR_ALIGN = -2,   /* a device buffer is not 256-byte aligned        */
     ZERO_ERR_CUDA = -3,    /* a CUDA launch or query failed                  */
     ZERO_ERR_STATE = -4,   /* call not valid for this layout's stage          */
-    ZERO_ERR_TIMEOUT = -5, /* reserved: no call waits on the device           */
+    ZERO_ERR_TIMEOUT = -5, /* reserved: no host call waits on the device      */
     ZERO_ERR_NOMEM = -6    /* host allocation of the layout object failed     */
 };
 
@@ -143,7 +143,10 @@ typedef struct zero_step_state {
     int32_t nonfinite;           /* OR of this step's reduce-scatter checks     */
     int32_t overflow;            /* last decided step overflowed                */
     int32_t apply;               /* last decided step applies the update        */
-    int32_t error;               /* device-detected error (0 = none)            */
+    int32_t error;               /* device-detected errors, OR of bits (0 = none):
+                                    1 = a bounded wait of a kernel on its own bulk
+                                    copies ran out; that CTA drained its copies and
+                                    stopped, so the step's results are incomplete */
     int32_t reserved[3];
 } zero_step_state;
 
@@ -386,7 +389,8 @@ zero_status_t zero_fused_step_noalloc(const zero_layout* L, const zero_adamw_hp*
                                       zero_stream_t stream);
 
 /* Cap on the CTAs of every later launch by this library (process-wide;
- * 0 = no cap: persistent grids of one full wave of CTAs).  For overlapping
+ * 0 = no cap: each kernel's own persistent grid, one full wave of CTAs or,
+ * where that measured faster on GB300, fewer CTAs per SM).  For overlapping
  * the library's memory-bound kernels with other work on another stream
  * (ZeRO-3 prefetch under a layer's compute): a full-wave grid occupies every
  * SM, so concurrent kernels would serialise behind it.  Results do not depend
