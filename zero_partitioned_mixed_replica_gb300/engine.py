@@ -279,23 +279,25 @@ class ZeroStep:
             B.zero_stage3_gather_layer(L, u, self.shard16_rows, rows[i % nb], comm)
             gathered[i].record(comm)
 
-        gather(0)
-        for i, (kind, u) in enumerate(uses):
-            if i + 1 < len(uses) and nb > 1:
-                gather(i + 1)                        # prefetch the next unit
-            comp.wait_event(gathered[i])
-            compute(kind, u, rows[i % nb])
-            used[i].record(comp)
-            if nb == 1 and i + 1 < len(uses):
-                gather(i + 1)
-            if kind == "bwd":
-                comm.wait_event(used[i])             # the unit's gradients exist after its backward
-                B.zero_fused_step(L, u, self.hp, self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
-                                  self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, self.workspace, comm)
-        B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, comm)
-        comp.wait_stream(comm)
-        if prev_cap is not None:
-            B.zero_set_max_ctas(prev_cap)
+        try:
+            gather(0)
+            for i, (kind, u) in enumerate(uses):
+                if i + 1 < len(uses) and nb > 1:
+                    gather(i + 1)                        # prefetch the next unit
+                comp.wait_event(gathered[i])
+                compute(kind, u, rows[i % nb])
+                used[i].record(comp)
+                if nb == 1 and i + 1 < len(uses):
+                    gather(i + 1)
+                if kind == "bwd":
+                    comm.wait_event(used[i])             # the unit's gradients exist after its backward
+                    B.zero_fused_step(L, u, self.hp, self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
+                                      self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, self.workspace, comm)
+            B.zero_grad_norm(L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, comm)
+        finally:
+            comp.wait_stream(comm)
+            if prev_cap is not None:                     # the cap is process-wide: always put it back
+                B.zero_set_max_ctas(prev_cap)
 
     # -- gradient accumulation over micro-batches ------------------------------------
     def micro_step(self, micro: int) -> None:
@@ -354,11 +356,13 @@ class ZeroStep:
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))
         old = self.stream
-        with torch.cuda.stream(side):
-            self.stream = side
-            with torch.cuda.graph(g, stream=side):
-                self.step()
-        self.stream = old
+        try:
+            with torch.cuda.stream(side):
+                self.stream = side
+                with torch.cuda.graph(g, stream=side):
+                    self.step()
+        finally:
+            self.stream = old
         torch.cuda.current_stream(self.device).wait_stream(side)
         return g
 
