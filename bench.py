@@ -98,13 +98,33 @@ def bytes_per_param(w, fused: bool, n_micro: int = 1) -> float:
     return 4 * nd + 24 + min(2 * nd, 8)
 
 
-def kernel_bytes(name: str, w, elems: int) -> float:
-    nd = w.n_d
-    per = {"reduce_scatter": 2 * nd + 4, "accumulate": 10 * nd,
+def kernel_bytes(name: str, w, elems: float, n_micro: int = 1) -> float:
+    """Algorithmic bytes of one launch of ``name`` over ``elems`` elements
+    (16-bit = 2 bytes).  Under micro-batching the reduce-scatter and the
+    ZeRO-1 accumulation average their first and later modes."""
+    nd, M = w.n_d, n_micro
+    rs = 2 * nd + 4
+    acc = 10 * nd
+    if M > 1:
+        rs = 4 * nd + 4 if w.stage == 1 else 2 * nd + 4 + 4 * (M - 1) / M   # later ones also read the fp32 shard
+        acc = (6 * nd + 10 * nd * (M - 1)) / M
+    per = {"reduce_scatter": rs, "accumulate": acc,
            "adamw": 4 + 24 + (2 * nd if w.stage != 3 else 2),
            "fused_step": 2 * nd + 24 + (2 * nd if w.stage != 3 else 2), "stage3_gather": 2 + 2 * nd,
            "allgather": 2 + 2 * nd, "grad_norm": 4 / 32}[name]
     return per * elems
+
+
+def elems_per_launch(name: str, w, psi_pad: int, launches_per_step: float, n_micro: int = 1) -> float:
+    """Elements one launch of ``name`` processes, on average over a step."""
+    M = n_micro
+    if name == "reduce_scatter":        # every micro-batch reduces the whole buffer (ZeRO-2/3)
+        return psi_pad * (M if w.stage != 1 else 1) / max(1.0, launches_per_step)
+    if name == "fused_step":
+        return psi_pad / max(1.0, launches_per_step)
+    if name == "stage3_gather":         # real elements, forward and backward, every micro-batch
+        return 2 * w.psi * M / max(1.0, launches_per_step)
+    return psi_pad                      # adamw, accumulate, allgather, grad_norm: the whole buffer
 
 
 def measured_peak():
@@ -585,20 +605,16 @@ def main():
     peak, peak_kind = measured_peak()
     roof = None
     if kern:
+        for name, k in kern.items():       # achieved GB/s of every kernel, algorithmic bytes
+            e = elems_per_launch(name, w, info.psi_pad, k["launches"] / args.steps, args.micro)
+            k["gbs"] = kernel_bytes(name, w, e, args.micro) / (k["avg_ms"] / 1e3) / 1e9
         dom = max(kern, key=lambda k: kern[k]["total_ms"])
-        if dom == "accumulate":
-            elems = info.psi_pad
-        elif dom in ("reduce_scatter", "fused_step"):
-            elems = info.psi_pad / max(1, kern[dom]["launches"] // args.steps)
-        elif dom == "stage3_gather":
-            elems = 2 * w.psi / max(1, kern[dom]["launches"] // args.steps)
-        else:
-            elems = info.psi_pad
-        ach = kernel_bytes(dom, w, elems) / (kern[dom]["avg_ms"] / 1e3) / 1e9
+        elems = elems_per_launch(dom, w, info.psi_pad, kern[dom]["launches"] / args.steps, args.micro)
+        ach = kernel_bytes(dom, w, elems, args.micro) / (kern[dom]["avg_ms"] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "peak_kind": peak_kind + " (copy bandwidth)",
                 "traffic": ncu_traffic(dom, args.workload),
-                "algorithmic_bytes_per_launch": kernel_bytes(dom, w, elems),
+                "algorithmic_bytes_per_launch": kernel_bytes(dom, w, elems, args.micro),
                 "avg_launch_ms": kern[dom]["avg_ms"]}
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -75,3 +75,32 @@ def test_reference_arm_nonzero_rank_exits_quietly():
     p = _run(["--impl", "reference", "--workload", "tiny", "--steps", "1"],
              {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("name,micro", [("gpt2_xl", 1), ("gpt2_small", 1), ("llama7b", 1), ("gpt2_xl", 4),
+                                        ("gpt2_small", 4), ("llama7b", 2), ("tiny", 3)])
+def test_per_kernel_bytes_add_up_to_the_step(name, micro):
+    # the per-kernel byte model behind the JSON line's "gbs" and roofline equals the per-step model
+    import bench
+    from oracle.layout import make_layout
+    from zero_partitioned_mixed_replica_gb300 import workloads
+    w = workloads.ALL[name]()
+    L = make_layout(w.numels, w.n_d, w.stage, bucket_elems=w.bucket_elems if w.stage != 3 else 0,
+                    unit_of_tensor=w.unit_of_tensor if w.stage == 3 else None)
+    fused = w.fused() and micro == 1
+    nb, U, M = len(L.buckets), len(L.units), micro
+    if w.stage == 3:
+        launches = {"stage3_gather": 2 * U * M, ("fused_step" if fused else "reduce_scatter"): U * M}
+    elif fused:
+        launches = {"fused_step": nb}
+    else:
+        launches = {"reduce_scatter": nb * (M if w.stage == 2 else 1)}
+        if w.stage == 1 and M > 1:
+            launches["accumulate"] = M
+    if not fused:
+        launches["adamw"] = 1
+    total = sum(n * bench.kernel_bytes(k, w, bench.elems_per_launch(k, w, L.psi_pad, n, M), M)
+                for k, n in launches.items())
+    expect = bench.bytes_per_param(w, fused, M) * L.psi_pad
+    gathered_pad = 2 * (2 + 2 * w.n_d) * M * (L.psi_pad - w.psi) if w.stage == 3 else 0   # gathers skip padding
+    assert abs(total + gathered_pad - expect) <= 1e-9 * expect, (total, expect)
