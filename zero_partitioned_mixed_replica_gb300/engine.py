@@ -121,7 +121,8 @@ class ZeroStep:
             raise ValueError("ZeRO-3 reduces per unit")
         L = B.zero_layout_init(self.numels, None, self.n_d, self.stage, self.pad_multiple, bucket_elems, self.dtype)
         info = B.zero_layout_query(L)
-        assert info.psi_pad == self.info.psi_pad and info.shard_len == self.info.shard_len
+        if info.psi_pad != self.info.psi_pad or info.shard_len != self.info.shard_len:   # cannot happen: padding ignores buckets
+            raise RuntimeError("re-bucketed layout changed the padded length")
         self.L, self.info, self.n_buckets = L, info, info.n_buckets
 
     # -- pointer lists ---------------------------------------------------------
@@ -160,7 +161,8 @@ class ZeroStep:
         """Scatter a flat fp32 master (Psi_pad, zero padding) into the rank
         shards, zero m and v, and set the 16-bit parameters to its
         round-to-nearest-even cast."""
-        assert flat_master.numel() == self.info.psi_pad
+        if flat_master.numel() != self.info.psi_pad:
+            raise ValueError("load_master needs Psi_pad = %d elements, got %d" % (self.info.psi_pad, flat_master.numel()))
         fm = flat_master.to(self.device, torch.float32)
         for u in self.units:
             for r in range(self.n_d):
@@ -367,6 +369,13 @@ class ZeroStep:
         return g
 
     # -- host input ----------------------------------------------------------------------
+    def _check_host(self, host: torch.Tensor, need_pinned: bool) -> None:
+        if tuple(host.shape) != tuple(self.grads.shape) or host.dtype != self.grads.dtype:
+            raise ValueError("host gradients must be %s %s, got %s %s"
+                             % (tuple(self.grads.shape), self.grads.dtype, tuple(host.shape), host.dtype))
+        if need_pinned and not host.is_pinned():
+            raise ValueError("overlapped host copies need pinned host memory")
+
     def step_from_host(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
         """One step whose N_d gradient replicas come from pinned host memory.
 
@@ -380,8 +389,7 @@ class ZeroStep:
         produced), with the host link standing in for backward.  Fused steps
         run per bucket here.
         The result is identical to ``upload_grads(host)`` then ``step()``."""
-        assert tuple(host.shape) == tuple(self.grads.shape) and host.dtype == self.grads.dtype
-        assert host.is_pinned(), "asynchronous host copies need pinned memory"
+        self._check_host(host, True)
         if getattr(self, "_copy_streams", None) is None:
             self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
         cur = self._s()
@@ -416,7 +424,7 @@ class ZeroStep:
         """Copy the N_d gradient replicas from (pinned) host memory, in chunks
         alternating over two copy streams (faster than one large copy on this
         part), ordered before the next library call on the step's stream."""
-        assert tuple(host.shape) == tuple(self.grads.shape) and host.dtype == self.grads.dtype
+        self._check_host(host, False)
         if getattr(self, "_copy_streams", None) is None:
             self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
         cur = self._s()

@@ -65,7 +65,8 @@ def grad_replica(numels: Sequence[int], offsets: Sequence[int], psi_pad: int, fm
     if out is None:
         out = torch.zeros(psi_pad, dtype=dt, device=device)
     else:
-        assert out.dtype == dt and out.numel() == psi_pad
+        if out.dtype != dt or out.numel() != psi_pad:
+            raise ValueError("out must hold Psi_pad elements of the gradient dtype")
         out.zero_()
     gen = _gen(out.device, _stream_seed(seed, _SALT_GRAD, rank, step))
     for t, (n, off) in enumerate(zip(numels, offsets)):
