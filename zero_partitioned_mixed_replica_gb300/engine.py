@@ -453,11 +453,21 @@ class ZeroStep:
         torch.cuda.synchronize(self.device)
         p16 = self._shard16_rows_view()
 
+        chunk = 64 << 20                       # bytes per staged device-to-host copy
+
         def dump(r):
-            with open(os.path.join(path, "rank%03d.bin" % r), "wb") as f:
-                for t in (self.master[r], self.m[r], self.v[r]):
-                    f.write(t.cpu().numpy().tobytes())
-                f.write(p16[r].contiguous().view(torch.int16).cpu().numpy().tobytes())
+            # one pinned staging buffer per writer; the file gets the staged bytes as they are
+            stage = torch.empty(chunk, dtype=torch.uint8, pin_memory=True)
+            view = stage.numpy()
+            stream = torch.cuda.Stream(self.device)
+            with open(os.path.join(path, "rank%03d.bin" % r), "wb") as f, torch.cuda.stream(stream):
+                for t in (self.master[r], self.m[r], self.v[r], p16[r].contiguous()):
+                    flat = t.view(torch.uint8)
+                    for off in range(0, flat.numel(), chunk):
+                        n = min(chunk, flat.numel() - off)
+                        stage[:n].copy_(flat[off:off + n], non_blocking=True)
+                        stream.synchronize()
+                        f.write(memoryview(view[:n]))
             return 14 * self.info.shard_len
 
         with ThreadPoolExecutor(max_workers=min(16, self.n_d)) as ex:
