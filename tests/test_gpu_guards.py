@@ -108,12 +108,12 @@ def _run(c: Case, steps: int, split: bool, micro: int = 1):
 RAGGED = [50_001, 7, 30_000, 333]
 
 
-@pytest.mark.parametrize("nd", [1, 2, 3, 8])
+@pytest.mark.parametrize("nd", [1, 2, 3, 8, 64])
 def test_guards_fused_zero2(nd):
     _run(Case(RAGGED, nd, 2, FMT_BF16, bucket_elems=4096 + 32), 2, split=False)
 
 
-@pytest.mark.parametrize("nd", [2, 5, 8])
+@pytest.mark.parametrize("nd", [2, 5, 8, 64])
 def test_guards_split_clip_fp16_unfused_allgather(nd):
     _run(Case(RAGGED, nd, 2, FMT_FP16, bucket_elems=8192, max_norm=0.1, loss_scale=1024.0, dynamic=True),
          2, split=True)

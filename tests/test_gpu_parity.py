@@ -346,3 +346,14 @@ def test_user_pad_multiple(stage, units):
              units=units, max_norm=0.05, pad_multiple=4 * 3 * 128)
     eng, zs, _ = run_parity(c, 2, use_gpu_clip=True)
     assert eng.info.q == 4 * 3 * 128 and eng.info.psi_pad % (4 * 3 * 128) == 0
+
+
+@pytest.mark.parametrize("n_d,stage", [(64, 2), (64, 1), (16, 2), (64, 3)])
+def test_split_clip_at_the_rank_limit(n_d, stage):
+    # ZERO_MAX_RANKS = 64: the runtime-N_d reduce-scatter, the TMA AdamW's 64 bulk stores per
+    # tile (ZeRO-1/2) or the shard-output update (ZeRO-3); fp16 with a dynamic scale and clip
+    units = [0, 1, 1, 2] if stage == 3 else None
+    c = Case([200_000, 7, 50_001, 3000], n_d, stage, FMT_FP16, bucket_elems=65_536 if stage != 3 else 0,
+             units=units, max_norm=0.05, loss_scale=1024.0, dynamic=True, per_tensor_scale=True)
+    _, _, hist = run_parity(c, 2, use_gpu_clip=True)
+    assert all(g["clip_coef"] < 1.0 for g, _ in hist)
