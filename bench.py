@@ -159,6 +159,24 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def host_mem_available():
+    """MemAvailable of this host in bytes (Linux /proc/meminfo), or None."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def e2e_fits(need_bytes: int, local_world: int, avail) -> bool:
+    """Whether every local rank can pin its own copy of the step's gradients
+    while keeping at least half of the host's available memory free."""
+    return avail is None or need_bytes * local_world <= avail // 2
+
+
 def host_link_gbs(host: torch.Tensor, dev_buf: torch.Tensor, stream) -> float:
     """Host-to-device rate of this box's link, measured just before the e2e
     leg: the better of two pinned copies of the whole gradient buffer into
@@ -362,7 +380,16 @@ def gpu_run(args, w, rank, world, local_rank):
             kern[name] = {"launches": len(d), "total_ms": sum(d), "avg_ms": sum(d) / len(d)}
     # --- e2e: host buffers, H2D of the step's gradients + D2H of the step result ----
     e2e = None
-    if args.e2e_steps > 0:
+    need = int(eng.grads.numel() * eng.grads.element_size())
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    avail = host_mem_available()
+    if args.e2e_steps > 0 and not e2e_fits(need, local_world, avail):
+        # every local rank pins its own copy of the step's gradients; more than half of the
+        # host's available memory in pinned pages would put the host at risk
+        e2e = {"value": None, "unit": "params/s",
+               "skipped": "host memory: %d ranks x %.1f GB pinned > half of %.1f GB available"
+                          % (local_world, need / 1e9, avail / 1e9)}
+    elif args.e2e_steps > 0:
         try:
             host_grads = torch.empty(tuple(eng.grads.shape), dtype=eng.grads.dtype, pin_memory=True)
             host_grads.copy_(eng.grads)

@@ -104,3 +104,13 @@ def test_per_kernel_bytes_add_up_to_the_step(name, micro):
     expect = bench.bytes_per_param(w, fused, M) * L.psi_pad
     gathered_pad = 2 * (2 + 2 * w.n_d) * M * (L.psi_pad - w.psi) if w.stage == 3 else 0   # gathers skip padding
     assert abs(total + gathered_pad - expect) <= 1e-9 * expect, (total, expect)
+
+
+def test_e2e_skips_when_pinned_copies_would_crowd_the_host():
+    import bench
+    assert bench.host_mem_available() is None or bench.host_mem_available() > 0
+    gb = 10 ** 9
+    assert bench.e2e_fits(25 * gb, 1, 199 * gb)          # 1.5B at N = 1 on a 199 GB host
+    assert bench.e2e_fits(25 * gb, 2, 199 * gb)
+    assert not bench.e2e_fits(25 * gb, 8, 199 * gb)      # 8 ranks would pin 200 GB
+    assert bench.e2e_fits(25 * gb, 8, None)              # unknown: no guard
