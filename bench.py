@@ -644,7 +644,7 @@ def main():
                 "algorithmic_bytes_per_launch": kernel_bytes(dom, w, elems, args.micro),
                 "avg_launch_ms": kern[dom]["avg_ms"]}
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu:   # the oracle baseline: rank 0 at N = 1 only
         sample = args.cpu_sample or default_sample(w)
         cb = oracle_timing(w, sample, min_seconds=args.cpu_seconds)
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
