@@ -643,11 +643,14 @@ def main():
                 "traffic": ncu_traffic(dom, args.workload),
                 "algorithmic_bytes_per_launch": kernel_bytes(dom, w, elems, args.micro),
                 "avg_launch_ms": kern[dom]["avg_ms"]}
+        if roof["traffic"] is not None:        # the same launch time over the ncu DRAM bytes
+            roof["achieved_by_ncu_bytes"] = roof["traffic"] / (kern[dom]["avg_ms"] / 1e3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:   # the oracle baseline: rank 0 at N = 1 only
         sample = args.cpu_sample or default_sample(w)
         cb = oracle_timing(w, sample, min_seconds=args.cpu_seconds)
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["gbs"] = cb["value"] * bpp / 1e9     # the host's rate in the step's algorithmic bytes
     if rank != 0:
         return
     line = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
