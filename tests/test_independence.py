@@ -24,7 +24,7 @@ def _imports(path):
         for ch in ast.iter_child_nodes(node):
             f = ch.name if isinstance(ch, (ast.FunctionDef, ast.AsyncFunctionDef)) else func
             if isinstance(ch, ast.Import):
-                out += [(a.name.split(".")[0], func) for a in ch.names]
+                out.extend((a.name.split(".")[0], func) for a in ch.names)
             elif isinstance(ch, ast.ImportFrom) and ch.module and ch.level == 0:
                 out.append((ch.module.split(".")[0], func))
             visit(ch, f)
