@@ -51,9 +51,12 @@ def test_oracle_never_imports_the_package():
 def test_oracle_is_run_only_where_allowed():
     allowed = {"bench.py": {"oracle_timing"}, "__graft_entry__.py": {"build", "smoke"}}
     for name, funcs in allowed.items():
+        seen = set()
         for mod, func in _imports(os.path.join(ROOT, name)):
             if mod == "oracle":
                 assert func in funcs, (name, func)
+                seen.add(func)
+        assert seen == funcs, (name, seen)      # the scan did find them
 
 
 def test_c_sources_include_nothing_from_the_other_side():
