@@ -410,21 +410,33 @@ def gpu_run(args, w, rank, world, local_rank):
             # link at 90-140 GB/s before settling at the link rate.
             for _ in range(max(3, args.warmup)):
                 e2e_step()
+            # the copies alone (same chunks on the same two streams), to read the e2e value against
+            copy_ms = []
+            for _ in range(2):
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                eng.upload_grads(host_grads)
+                c1.record(stream)
+                c1.synchronize()
+                copy_ms.append(c0.elapsed_time(c1))
             torch.cuda.synchronize(dev)
             if world > 1:
                 dist.barrier()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.e2e_steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+            evs[0].record(stream)
+            for i in range(args.e2e_steps):
                 e2e_step()
-            b.record(stream)
+                evs[i + 1].record(stream)
             torch.cuda.synchronize(dev)
+            a, b = evs[0], evs[-1]
             ems = max_over_ranks(a.elapsed_time(b), world)
             e2e = {"value": world * w.psi * args.e2e_steps / (ems / 1e3), "unit": "params/s",
                    "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()) * args.micro,
                    "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps,
                    "warmup_steps": max(3, args.warmup), "host_link_gbs": link_gbs,
-                   "h2d_floor_ms": int(eng.grads.numel() * eng.grads.element_size()) * args.micro / link_gbs / 1e6}
+                   "h2d_floor_ms": int(eng.grads.numel() * eng.grads.element_size()) * args.micro / link_gbs / 1e6,
+                   "copy_only_ms": min(copy_ms),
+                   "ms_each": [round(evs[i].elapsed_time(evs[i + 1]), 2) for i in range(args.e2e_steps)]}
             del host_grads
         except RuntimeError as ex:
             e2e = {"value": None, "unit": "params/s", "error": str(ex)[:200]}
