@@ -10,7 +10,13 @@ whole hot path over one batch of synthetic gradients resident in HBM:
 step decision -> sharded AdamW with the all-gather fused in.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gpt2_xl|gpt2_small|llama7b|tiny]
+                  [--workload gpt2_xl|gpt2_small|llama7b|gpt2_medium|tiny|gpt2_xl_block|llama7b_block]
+                  [--graph] [--whole-buffer] [--micro M] [--sweep] [--prefetch] [--checkpoint DIR]
+
+The e2e value repeats the step with the gradient replicas copied every step
+from pinned host memory (ZeroStep.step_from_host: per-bucket copies overlapped
+with the reduce-scatter) and the step state read back, after untimed warm-up
+steps; it reports the host link's rate and the copies' time beside it.
 
 Under torchrun (N > 1) every rank runs its own independent replica of the
 step on its own GPU (the simulated ranks live inside one GPU; there is no
