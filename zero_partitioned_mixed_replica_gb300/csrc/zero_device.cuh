@@ -275,11 +275,21 @@ __device__ __forceinline__ void adamw1(float& p, float& m, float& v, float g, co
 
 // ----------------------------------------------------------------------------
 // Bulk asynchronous copies (TMA, 1-D form) and mbarriers, inline PTX.
-// Every wait on an mbarrier is bounded: after kWaitLimit failed polls the
-// caller records ZERO_DEVERR_WAIT_TIMEOUT in the step state and unwinds.
+// Every wait on an mbarrier is bounded in time: once kWaitLimitNs of the
+// global timer have passed (or, as a backstop, kWaitMaxPolls polls) the wait
+// gives up, and the caller records ZERO_DEVERR_WAIT_TIMEOUT in the step state
+// and unwinds.  A poll (mbarrier.try_wait) may itself suspend the thread for
+// a system-dependent time, so a poll count alone does not bound the time.
 // ----------------------------------------------------------------------------
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr uint32_t kWaitMaxPolls = 1u << 26;
 constexpr int32_t ZERO_DEVERR_WAIT_TIMEOUT = 1;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -315,8 +325,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait; false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;  // the common case: no timer read
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
     return false;
 }
 // global -> this CTA's shared memory, completion counted on `bar` (bytes).
