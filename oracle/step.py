@@ -215,6 +215,19 @@ def adamw_inplace(p: np.ndarray, m: np.ndarray, v: np.ndarray, g: np.ndarray,
 # Step state: loss scale, step counter, skip decision, norm and clip
 # ---------------------------------------------------------------------------
 
+def norm_and_clip(sumsq: float, max_norm: float) -> Tuple[float, float]:
+    """Global norm and clip coefficient from the global sum of squares.
+
+    The norm is global across shards ("ZeRO-3 核心流程：把参数也切开的那一档",
+    坑 1: every rank must clip with the same coefficient).  The coefficient
+    follows the common global-norm clipping convention: c = max_norm /
+    (norm + 1e-6) in binary64, clamped to at most 1, rounded once to
+    binary32; max_norm <= 0 disables clipping (c = 1)."""
+    norm = math.sqrt(sumsq)
+    clip = _f32(min(1.0, max_norm / (norm + CLIP_EPS))) if max_norm > 0 else 1.0
+    return norm, clip
+
+
 @dataclass
 class StepState:
     loss_scale: float = 1.0
@@ -240,8 +253,7 @@ class StepState:
             if self.dynamic:
                 self.loss_scale = max(1.0, self.loss_scale / 2.0)
         else:
-            norm = math.sqrt(sumsq)
-            clip = _f32(min(1.0, max_norm / (norm + CLIP_EPS))) if max_norm > 0 else 1.0
+            norm, clip = norm_and_clip(sumsq, max_norm)
             if clip_override is not None:
                 clip = _f32(clip_override)
             apply = True

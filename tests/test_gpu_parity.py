@@ -357,3 +357,27 @@ def test_split_clip_at_the_rank_limit(n_d, stage):
              units=units, max_norm=0.05, loss_scale=1024.0, dynamic=True, per_tensor_scale=True)
     _, _, hist = run_parity(c, 2, use_gpu_clip=True)
     assert all(g["clip_coef"] < 1.0 for g, _ in hist)
+
+
+@pytest.mark.parametrize("stage,fmt,loss_scale", [(2, FMT_BF16, 1.0), (2, FMT_FP16, 65536.0),
+                                                  (3, FMT_FP16, 1024.0)])
+def test_split_clip_clamp_branch_equals_unclipped(stage, fmt, loss_scale):
+    # max_norm far above the global norm ("ZeRO-3 核心流程", 坑 1: one coefficient on every rank):
+    # the clamp gives c = 1.0 exactly, on the GPU and in the oracle's own decision, and the step
+    # equals the same step without clipping, bit for bit
+    units = Z3_UNITS if stage == 3 else None
+    numels = Z3_NUMELS if stage == 3 else [120_000, 7, 50_001]
+    kw = dict(bucket_elems=32_768 if stage != 3 else 0, units=units, loss_scale=loss_scale,
+              dynamic=loss_scale != 1.0, per_tensor_scale=True)
+    c = Case(numels, 4, stage, fmt, max_norm=1e3, **kw)
+    e1, _, hist = run_parity(c, 3, use_gpu_clip=False)
+    assert all(g["clip_coef"] == 1.0 and o["clip"] == 1.0 and o["norm"] < 1e3 for g, o in hist)
+    assert all(0.0 < g["grad_norm"] for g, _ in hist)
+    c0 = Case(numels, 4, stage, fmt, max_norm=0.0, **kw)
+    e0, _, _ = run_parity(c0, 3)
+    for name in ("master", "m", "v"):
+        assert torch.equal(getattr(e1, name), getattr(e0, name)), name
+    if stage == 3:
+        assert torch.equal(e1.shard16, e0.shard16)
+    else:
+        assert torch.equal(e1.params, e0.params)
