@@ -146,7 +146,11 @@ typedef struct zero_step_state {
     int32_t error;               /* device-detected errors, OR of bits (0 = none):
                                     1 = a bounded wait of a kernel on its own bulk
                                     copies ran out; that CTA drained its copies and
-                                    stopped, so the step's results are incomplete */
+                                    stopped, so the step's results are incomplete;
+                                    2 = also, while draining, one of those copies
+                                    did not land within 4 more bounded waits: the
+                                    CTA exited with it possibly still in flight,
+                                    so treat the context as unreliable */
     int32_t reserved[3];
 } zero_step_state;
 
@@ -289,6 +293,22 @@ zero_status_t zero_adamw_shard_step(const zero_layout* L, const zero_adamw_hp* h
 zero_status_t zero_allgather_params(const zero_layout* L, const void* const* param16_shards,
                                     void* const* param16_full, zero_stream_t stream);
 
+/* The 16-bit parameters of the current fp32 master, without an update:
+ * the cast of [L5] §3 step 2 ("cast the fp32 shard to BF16 in place") and,
+ * for ZERO_OUT_FULL_REPLICAS, the all-gather of step 3.  For initialising
+ * the 16-bit parameters from a loaded master (and after a checkpoint load).
+ *   master:       N_d device pointers to fp32 shards (S each), read only.
+ *   param16_out:  ZERO_OUT_FULL_REPLICAS (ZeRO-1/2): N_d full replicas
+ *                 (Psi_pad each); element r*S + j of every replica receives
+ *                 round-to-nearest-even 16-bit(master[r][j]).
+ *                 ZERO_OUT_SHARDS: N_d 16-bit shards (S each); shard r
+ *                 receives the cast of master[r].  ZeRO-3 requires it.
+ * Padding casts its zeros to +0.  One kernel; asynchronous on `stream`.
+ * Errors: NULL/misaligned pointers, unknown out_kind (ZERO_ERR_INVALID /
+ * ZERO_ERR_ALIGN); stage 0, or ZeRO-3 with full replicas (ZERO_ERR_STATE). */
+zero_status_t zero_cast_params(const zero_layout* L, const float* const* master,
+                               void* const* param16_out, int32_t out_kind, zero_stream_t stream);
+
 /* ZeRO-3 gather of unit `unit` into every rank's transient buffer ([L5]
  * Fig. 5-1; [RN] §3.1 and §4.3; [Z3] §2 steps 1-2): transient[k][i] =
  * param16_shards[r][S_u_base + i - r*S_u] for i in [0, real_u), r = i / S_u,
@@ -314,6 +334,75 @@ zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
                               float* const* master, float* const* m, float* const* v,
                               zero_step_state* st, void* const* param16_out, int32_t out_kind,
                               void* workspace, zero_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* The whole step in one call                                                */
+/* ------------------------------------------------------------------------ */
+/* Buffers and settings of one step, for zero_step and zero_step_from_host.
+ * Every pointer array holds N_d device pointers (256-byte aligned); the
+ * library reads the arrays during the call only. */
+typedef struct zero_step_args {
+    const zero_adamw_hp* hp;            /* host pointer, read during the call */
+    double max_norm;                    /* split step: clip threshold (<= 0: no clip) */
+    int32_t fused;                      /* 1: zero_fused_step per bucket/unit + norm report
+                                           (no clip, no loss-scale skip); 0: split step */
+    int32_t per_bucket;                 /* fused ZeRO-1/2: 1 = one launch per bucket,
+                                           0 = one launch over the whole buffer */
+    const void* const* grad_replicas;   /* 16-bit, Psi_pad each (zero_step_from_host:
+                                           the device destinations of the copies) */
+    float* const* master;               /* fp32 shards, S each */
+    float* const* m;
+    float* const* v;
+    float* const* grad_shards;          /* split step: fp32 shards (S); fused: unused */
+    void* const* param16_full;          /* ZeRO-1/2: full 16-bit replicas; ZeRO-3: unused */
+    void* const* param16_shards;        /* ZeRO-3: 16-bit shards (S).  ZeRO-1/2 split step:
+                                           NULL = the update writes param16_full directly
+                                           (all-gather fused), else it writes these shards
+                                           and zero_allgather_params follows */
+    void* const* transient;             /* ZeRO-3: transient unit buffers (largest unit) */
+    zero_step_state* state;             /* device */
+    void* workspace;                    /* device, zero_layout_info.workspace_bytes */
+} zero_step_args;
+
+/* One whole step with the gradient replicas resident in device memory, in the
+ * pages' call order ([ML] "梯度桶化"; [RN] §4.1-§4.3; [L5] §3 and Fig. 5-1;
+ * [Z3] §2):
+ *   ZeRO-1/2 split: zero_reduce_scatter for every bucket, last bucket first
+ *     -> zero_grad_norm(max_norm, DECIDE) -> zero_adamw_shard_step (full
+ *     replicas, or shards + zero_allgather_params);
+ *   ZeRO-1/2 fused: zero_fused_step per bucket, last first (or once over the
+ *     buffer) -> zero_grad_norm(AFTER_FUSED);
+ *   ZeRO-3: zero_stage3_gather_layer for units 0..U-1 (forward), then for
+ *     u = U-1..0: gather u again and zero_fused_step(u) (fused) or
+ *     zero_reduce_scatter(u) (split, followed by the norm and the shard
+ *     update after the loop).
+ * Asynchronous on `stream`; allocates nothing; captures into a CUDA graph
+ * like the calls it issues.  Errors: those of the calls it issues (the first
+ * failing call stops the step and its status is returned); inconsistent
+ * arguments (fused with max_norm > 0, missing buffers for the stage) give
+ * ZERO_ERR_INVALID before any launch. */
+zero_status_t zero_step(const zero_layout* L, const zero_step_args* args, zero_stream_t stream);
+
+/* zero_step with the N_d gradient replicas in host memory.  host_grads: N_d
+ * host pointers, Psi_pad 16-bit elements each (page-locked memory lets the
+ * copies overlap the step; pageable memory is correct but copies in stages).
+ * Each bucket's range (ZeRO-3: each unit's) of every replica is copied into
+ * args->grad_replicas by cudaMemcpyAsync, chunk_elems elements at a time
+ * (<= 0: 2^27), alternating over two copy streams that the library owns (one
+ * pair per device, created at the first call and kept until exit), in the
+ * order the step consumes the buckets; the step's first reading launch of
+ * each bucket waits only for that bucket's copies, so later buckets cross the
+ * host link while earlier ones are reduced ([RN] §4.1-§4.2: a bucket is
+ * reduced as soon as it is filled).  The copies start after the work already
+ * queued on `stream` (the previous step reads the same device replicas).
+ * host_state: host pointer to sizeof(zero_step_state) bytes, or NULL; the
+ * step state is copied there at the end of the step, on `stream`.
+ * Asynchronous: synchronise `stream` before reading host_state or reusing
+ * host_grads.  Calls on one device are serialised by a library lock (they
+ * share the copy streams and events). */
+zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* args,
+                                  const void* const* host_grads, int64_t chunk_elems, void* host_state,
+                                  zero_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Gradient accumulation over M micro-batches per optimizer step             */
@@ -374,8 +463,10 @@ zero_status_t zero_reduce_scatter_micro(const zero_layout* L, int32_t bucket_or_
  *   - Psi_pad must not exceed ZERO_NOALLOC_MAX_ELEMS, else ZERO_ERR_INVALID
  *     (nothing is launched).  Stage 0: ZERO_ERR_STATE.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture begins.
+ *     that device current) and caches it with the id of the current context;
+ *     make that first call before any stream capture begins.  A later call
+ *     under another context of that device (after cudaDeviceReset) looks the
+ *     address up again.
  *   - All calls share the array and it keeps the last call's contents;
  *     nothing needs clearing, because each call writes every slot before it
  *     reads it.  Calls that overlap on the GPU (other streams, other host

@@ -175,3 +175,37 @@ def test_binding_refuses_pointer_lists_of_the_wrong_length():
     with pytest.raises(B.ZeroError) as e:      # NULL array: rejected by the library itself
         B.zero_allgather_params(L, None, [FAKE] * 4, 0)
     assert e.value.status == B.ZERO_ERR_INVALID
+
+
+def test_executor_and_cast_validate_before_launch():
+    L = B.zero_layout_init([1000, 24], None, 2, 2, 0, 0, B.ZERO_BF16)
+    L3 = B.zero_layout_init([1000, 24], [0, 1], 2, 3, 0, 0, B.ZERO_BF16)
+    L0 = B.zero_layout_init([1000, 24], None, 2, 0, 0, 0, B.ZERO_BF16)
+    two = [FAKE, FAKE]
+    hp = B.zero_adamw_hp(lr=1e-3, eps=1e-8, weight_decay=0.0)
+
+    def status(fn, *a):
+        with pytest.raises(B.ZeroError) as e:
+            fn(*a)
+        return e.value.status
+
+    def args(Lx, fused, max_norm=0.0, gshard=two, full=two, shards=None, transient=None, grads=two):
+        return B.StepArgs(Lx, hp, max_norm, fused, True, grads, two, two, two, gshard, full, shards, transient,
+                          FAKE, FAKE)
+
+    assert status(B.zero_step, L, args(L, True, max_norm=1.0), 0) == B.ZERO_ERR_INVALID     # fused cannot clip
+    assert status(B.zero_step, L, args(L, False, gshard=None), 0) == B.ZERO_ERR_INVALID    # split needs shards
+    assert status(B.zero_step, L, args(L, False, full=None), 0) == B.ZERO_ERR_INVALID      # ZeRO-2 needs replicas
+    assert status(B.zero_step, L, args(L, True, shards=two), 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_step, L3, args(L3, True, full=None, shards=two), 0) == B.ZERO_ERR_INVALID  # no transient
+    assert status(B.zero_step, L3, args(L3, True, full=None, transient=two), 0) == B.ZERO_ERR_INVALID  # no shards
+    assert status(B.zero_step, L0, args(L0, False), 0) == B.ZERO_ERR_STATE
+    # the first call the executor issues validates its own pointers before launching
+    assert status(B.zero_step, L, args(L, False, grads=[FAKE, MIS]), 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_step_from_host, L, args(L, False), None, 0, None, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_step_from_host, L, args(L, False), [FAKE, 0], 0, None, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_step_from_host, L, args(L, True, max_norm=0.5), two, 0, None, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_cast_params, L3, two, two, B.ZERO_OUT_FULL_REPLICAS, 0) == B.ZERO_ERR_STATE
+    assert status(B.zero_cast_params, L, two, two, 5, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_cast_params, L, [FAKE, MIS], two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_cast_params, L0, two, two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_STATE

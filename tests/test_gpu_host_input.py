@@ -1,9 +1,10 @@
-"""Steps whose gradient replicas come from pinned host memory
-(``ZeroStep.step_from_host``): per-bucket (ZeRO-3: per-unit) copies on two
-copy streams, each reduce-scatter or fused update ordered after its own range
-only.  Checked against the oracle bit for bit, on layouts whose buckets
-straddle shards, with chunks smaller than a bucket, and against the
-device-resident step."""
+"""Steps whose gradient replicas come from pinned host memory, through the
+library's zero_step_from_host (``ZeroStep.step_from_host``): per-bucket
+(ZeRO-3: per-unit) copies on the library's two copy streams, each
+reduce-scatter or fused update ordered after its own range only, and the
+step state copied back to host memory inside the call.  Checked against the
+oracle bit for bit, on layouts whose buckets straddle shards, with chunks
+smaller than a bucket, and against the device-resident step."""
 import pytest
 import torch
 
@@ -31,7 +32,8 @@ def test_host_input_zero2_fp16_scaler_overflow():
 
 def test_host_input_zero1_fused_per_bucket():
     c = Case([40_000, 33, 77_777, 5], 5, 1, FMT_BF16, bucket_elems=16_384, per_tensor_scale=True)
-    run_parity(c, 2, host_input=True, per_bucket=False)   # step_from_host runs per bucket regardless
+    run_parity(c, 2, host_input=True, per_bucket=False)   # one fused launch after every bucket's copies
+    run_parity(c, 2, host_input=True, per_bucket=True)
 
 
 def test_host_input_garbage_padding():
@@ -51,3 +53,21 @@ def test_host_input_equals_device_step():
     e2, _, _ = run_parity(c, 2, use_gpu_clip=True)
     assert torch.equal(e1.master, e2.master) and torch.equal(e1.params, e2.params)
     assert torch.equal(e1.m, e2.m) and torch.equal(e1.v, e2.v)
+
+
+def test_host_state_read_back_in_the_call():
+    from tests.test_gpu_parity import _engine
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_FP16, bucket_elems=32_768, max_norm=1.0, loss_scale=1024.0,
+             dynamic=True, per_tensor_scale=True)
+    L = c.layout()
+    eng = _engine(c)
+    eng.load_master(torch.from_numpy(c.master0(L)))
+    host = torch.empty(tuple(eng.grads.shape), dtype=eng.grads.dtype, pin_memory=True)
+    out = torch.zeros(96, dtype=torch.uint8).pin_memory()
+    for s in (1, 2):
+        for r, g in enumerate(c.grads_torch(L, s, 1024.0)):
+            host[r].copy_(g)
+        eng.step_from_host(host, state_out=out)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(out, eng.state.cpu())
+        assert eng.read_state()["t"] == s

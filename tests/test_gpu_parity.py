@@ -381,3 +381,77 @@ def test_split_clip_clamp_branch_equals_unclipped(stage, fmt, loss_scale):
         assert torch.equal(e1.shard16, e0.shard16)
     else:
         assert torch.equal(e1.params, e0.params)
+
+
+@pytest.mark.parametrize("n_d,stage,fmt", [(3, 2, FMT_BF16), (8, 1, FMT_FP16), (5, 3, FMT_FP16), (64, 2, FMT_BF16)])
+def test_cast_params_matches_oracle_cast(n_d, stage, fmt):
+    # zero_cast_params: the RNE cast of the master ("第 5 课" §3 step 2) into every replica (ZeRO-1/2,
+    # with the all-gather of step 3) or the rank's shard (ZeRO-3), against the oracle's encoder;
+    # the master holds fp16 subnormals, values at and beyond 65504, RNE midpoints and signed zeros
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    units = [0, 1, 1, 2] if stage == 3 else None
+    c = Case([40_000, 7, 33_001, 999], n_d, stage, fmt, units=units)
+    L = c.layout()
+    m0 = c.master0(L)
+    rng = np.random.default_rng(3)
+    special = np.array([6e-8, -6e-8, 5.96e-8, 1e-5, -3.1e-5, 65504.0, 65519.0, 65520.0, -7e4, 1e30, -0.0,
+                        1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8], np.float32)
+    real = np.concatenate([np.arange(o, o + n) for o, n in zip(L.tensor_offsets, L.numels)])
+    idx = rng.choice(real, size=special.size * 40, replace=False)
+    m0[idx] = np.tile(special, 40)
+    eng = _engine(c)
+    Bd.zero_launch_count(reset=True)
+    eng.load_master(torch.from_numpy(m0))
+    torch.cuda.synchronize()
+    assert Bd.zero_launch_count() == 1
+    zs = ZeroSimulation(L, m0, c.fmt, HP)
+    if stage == 3:
+        assert np.array_equal(_u16(eng.flat("shard16")), zs.flat("shard16"))
+    else:
+        for r in range(n_d):
+            assert np.array_equal(_u16(eng.params[r]), zs.params16[r]), r
+    # the layout's padding casts to +0
+    pad = np.ones(L.psi_pad, bool)
+    pad[real] = False
+    if stage != 3:
+        assert not _u16(eng.params[0])[pad].any()
+
+
+@pytest.mark.parametrize("mode", ["z2_fused_bucket", "z2_fused_whole", "z2_split_clip_fp16", "z1_split_unfused_ag",
+                                  "z3_fused", "z3_split_fp16"])
+def test_native_executor_equals_call_by_call(mode):
+    # zero_step (the library issues the step's calls) against the same calls issued one by one
+    # from Python (the path the per-kernel timers use): bit-identical state after 3 steps
+    kw = {"z2_fused_bucket": dict(n_d=4, stage=2, fmt=FMT_BF16, eng=dict(per_bucket=True)),
+          "z2_fused_whole": dict(n_d=4, stage=2, fmt=FMT_BF16, eng=dict(per_bucket=False)),
+          "z2_split_clip_fp16": dict(n_d=8, stage=2, fmt=FMT_FP16, max_norm=0.05, loss_scale=4096.0, dynamic=True,
+                                     inf_step=2, inf_rank=5, eng={}),
+          "z1_split_unfused_ag": dict(n_d=3, stage=1, fmt=FMT_BF16, max_norm=0.05, eng=dict(fuse_allgather=False)),
+          "z3_fused": dict(n_d=2, stage=3, fmt=FMT_BF16, eng={}),
+          "z3_split_fp16": dict(n_d=4, stage=3, fmt=FMT_FP16, max_norm=0.01, loss_scale=256.0, dynamic=True,
+                                eng={})}[mode]
+    ekw = kw.pop("eng")
+    n_d, stage, fmt = kw.pop("n_d"), kw.pop("stage"), kw.pop("fmt")
+    z3 = stage == 3
+    c = Case(Z3_NUMELS if z3 else [120_000, 7, 50_001], n_d, stage, fmt, bucket_elems=0 if z3 else 32_768,
+             units=Z3_UNITS if z3 else None, per_tensor_scale=True, **kw)
+    L = c.layout()
+    a, b = _engine(c, **ekw), _engine(c, **ekw)
+    m0 = torch.from_numpy(c.master0(L))
+    a.load_master(m0)
+    b.load_master(m0)
+    b.timers = {}                       # the Python call-by-call sequencer
+    for s in range(1, 4):
+        reps = c.grads_torch(L, s, a.read_state()["loss_scale"])
+        for r, g in enumerate(reps):
+            a.grads[r].copy_(g.cuda())
+            b.grads[r].copy_(g.cuda())
+        a.step()
+        b.step()
+    torch.cuda.synchronize()
+    assert b.timers and all(len(v) > 0 for v in b.timers.values())
+    for name in ("master", "m", "v", "state"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert torch.equal(a.shard16, b.shard16) if z3 else torch.equal(a.params, b.params)
+    if mode == "z2_split_clip_fp16":
+        assert a.read_state()["skipped"] == 1

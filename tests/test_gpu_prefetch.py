@@ -1,8 +1,8 @@
 """ZeRO-3 prefetch/overlap on the GPU: with the unit gathers on a second
 stream overlapping a stand-in layer compute, the step's results equal the
-sequential step bit for bit, and every compute saw exactly the unit's
-previous 16-bit parameters (integer checksums of the transient buffers against
-the oracle), for 1, 2 and 3 live units."""
+sequential step and the oracle's ZeRO-3 simulation bit for bit, and every
+compute saw exactly the unit's previous 16-bit parameters (integer checksums
+of the transient buffers against the oracle), for 1, 2 and 3 live units."""
 import numpy as np
 import pytest
 import torch
@@ -69,3 +69,12 @@ def test_overlapped_equals_sequential_and_sees_previous_params(live, ctas):
         for name in ("master", "m", "v", "shard16"):
             assert torch.equal(getattr(ovl, name), getattr(seq, name)), (name, s)
         assert torch.equal(ovl.state, seq.state)
+        # and against the oracle, not only against the sequential engine
+        for name in ("master", "m", "v"):
+            assert np.array_equal(ovl.flat(name).cpu().numpy().view(np.uint32), zs.flat(name).view(np.uint32)), \
+                (name, s)
+        assert np.array_equal(ovl.flat("shard16").view(torch.int16).cpu().numpy().view(np.uint16),
+                              zs.flat("shard16")), s
+        st, o = ovl.read_state(), zs.state.history[-1]
+        assert (st["t"], st["overflow"]) == (o["t"], o["overflow"])
+        assert abs(st["grad_norm"] - o["norm"]) <= 1e-9 * o["norm"]

@@ -36,9 +36,10 @@ ZERO_NORM_AFTER_FUSED = 1
 EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero_layout_unit",
             "zero_layout_tensor_offset", "zero_layout_destroy", "zero_state_init",
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
-            "zero_allgather_params", "zero_stage3_gather_layer", "zero_fused_step",
+            "zero_allgather_params", "zero_cast_params", "zero_stage3_gather_layer", "zero_fused_step",
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
-            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_set_max_ctas",
+            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_step_from_host",
+            "zero_set_max_ctas",
             "zero_last_error", "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
@@ -81,6 +82,34 @@ class zero_adamw_hp(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
 
 
+class zero_step_args(ctypes.Structure):
+    _fields_ = [("hp", ctypes.POINTER(zero_adamw_hp)), ("max_norm", ctypes.c_double),
+                ("fused", ctypes.c_int32), ("per_bucket", ctypes.c_int32)] + \
+               [(n, ctypes.POINTER(ctypes.c_void_p)) for n in
+                ("grad_replicas", "master", "m", "v", "grad_shards", "param16_full", "param16_shards",
+                 "transient")] + \
+               [("state", ctypes.c_void_p), ("workspace", ctypes.c_void_p)]
+
+
+class StepArgs:
+    """A filled ``zero_step_args`` that keeps its pointer arrays and
+    hyperparameters alive as long as it lives."""
+
+    def __init__(self, L: "Layout", hp: zero_adamw_hp, max_norm: float, fused: bool, per_bucket: bool,
+                 grad_replicas, master, m, v, grad_shards, param16_full, param16_shards, transient, st,
+                 workspace):
+        self._keep = [hp]
+        self.args = zero_step_args(hp=ctypes.pointer(hp), max_norm=float(max_norm), fused=int(bool(fused)),
+                                   per_bucket=int(bool(per_bucket)), state=_addr(st), workspace=_addr(workspace))
+        for name, xs in (("grad_replicas", grad_replicas), ("master", master), ("m", m), ("v", v),
+                         ("grad_shards", grad_shards), ("param16_full", param16_full),
+                         ("param16_shards", param16_shards), ("transient", transient)):
+            arr = _ptrs(xs, L)
+            if arr is not None:
+                self._keep.append(arr)
+                setattr(self.args, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
+
+
 assert ctypes.sizeof(zero_step_state) == 96
 
 _lib = None
@@ -108,6 +137,7 @@ def lib():
         "zero_grad_norm": [P, dbl, i32, P, P, P],
         "zero_adamw_shard_step": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
         "zero_allgather_params": [P, PP, PP, P],
+        "zero_cast_params": [P, PP, PP, i32, P],
         "zero_stage3_gather_layer": [P, i32, PP, PP, P],
         "zero_fused_step": [P, i32, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P, P],
         "zero_fused_step_noalloc": [P, ctypes.POINTER(zero_adamw_hp), PP, PP, PP, PP, P, PP, i32, P],
@@ -115,6 +145,8 @@ def lib():
         "zero_accumulate_grads": [P, i32, PP, PP, P],
         "zero_reduce_scatter_accumulated": [P, i32, PP, PP, i32, P, P, P],
         "zero_reduce_scatter_micro": [P, i32, i32, i32, PP, PP, P, P, P],
+        "zero_step": [P, ctypes.POINTER(zero_step_args), P],
+        "zero_step_from_host": [P, ctypes.POINTER(zero_step_args), PP, i64, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -254,6 +286,10 @@ def zero_allgather_params(L: Layout, param16_shards, param16_full, stream=None) 
     _check(lib().zero_allgather_params(L, _ptrs(param16_shards, L), _ptrs(param16_full, L), _stream(stream)))
 
 
+def zero_cast_params(L: Layout, master, param16_out, out_kind: int, stream=None) -> None:
+    _check(lib().zero_cast_params(L, _ptrs(master, L), _ptrs(param16_out, L), out_kind, _stream(stream)))
+
+
 def zero_stage3_gather_layer(L: Layout, unit: int, param16_shards, transient, stream=None) -> None:
     _check(lib().zero_stage3_gather_layer(L, unit, _ptrs(param16_shards, L), _ptrs(transient, L), _stream(stream)))
 
@@ -295,6 +331,18 @@ def zero_reduce_scatter_micro(L: Layout, bucket_or_unit: int, micro: int, n_micr
                               st, workspace, stream=None) -> None:
     _check(lib().zero_reduce_scatter_micro(L, bucket_or_unit, micro, n_micro, _ptrs(grad_replicas, L),
                                            _ptrs(acc_shards, L), _addr(st), _addr(workspace), _stream(stream)))
+
+
+def zero_step(L: Layout, args: StepArgs, stream=None) -> None:
+    _check(lib().zero_step(L, ctypes.byref(args.args), _stream(stream)))
+
+
+def zero_step_from_host(L: Layout, args: StepArgs, host_grads, chunk_elems: int = 0, host_state=None,
+                        stream=None) -> None:
+    """host_grads: one host pointer (or CPU tensor) per rank; host_state: a
+    CPU tensor / address of 96 bytes, or None."""
+    _check(lib().zero_step_from_host(L, ctypes.byref(args.args), _ptrs(host_grads, L), int(chunk_elems),
+                                     _addr(host_state), _stream(stream)))
 
 
 def zero_set_max_ctas(n: int) -> int:

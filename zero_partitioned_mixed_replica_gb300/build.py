@@ -21,7 +21,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero.so")
 
 SOURCES = ["zero_layout.cpp", "zero_rs.cu", "zero_adamw.cu", "zero_norm.cu", "zero_gather.cu",
-           "zero_noalloc.cu", "zero_accum.cu"]
+           "zero_noalloc.cu", "zero_accum.cu", "zero_exec.cpp"]
 HEADERS = ["zero_internal.h", "zero_device.cuh", "zero_launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

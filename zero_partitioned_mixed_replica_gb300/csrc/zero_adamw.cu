@@ -152,10 +152,18 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     if (tid == 0) {
         if (s_abort) {
             // After a timed-out wait on tile s_stop, let the loads still in
-            // flight (tiles s_stop .. s_stop + STAGES - 1) land, each wait
-            // bounded again, before the CTA gives up its shared memory.
+            // flight (tiles s_stop .. s_stop + STAGES - 1) land before the CTA
+            // gives up its shared memory: up to kDrainTries bounded waits per
+            // tile.  A tile that still has not landed is reported with
+            // ZERO_DEVERR_DRAIN_TIMEOUT; the CTA then exits with that copy
+            // possibly outstanding.
             const uint32_t k0 = s_stop, k1 = min(count, k0 + (uint32_t)STAGES);
-            for (uint32_t j = k0; j < k1; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u);
+            for (uint32_t j = k0; j < k1; ++j) {
+                bool landed = false;
+                for (int tries = 0; tries < kDrainTries && !landed; ++tries)
+                    landed = mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u);
+                if (!landed) atomicOr(&a.st->error, ZERO_DEVERR_DRAIN_TIMEOUT);
+            }
         }
         bulk_wait_all<0>();
     }

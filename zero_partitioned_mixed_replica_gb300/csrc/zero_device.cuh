@@ -284,6 +284,11 @@ __device__ __forceinline__ void adamw1(float& p, float& m, float& v, float g, co
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr uint32_t kWaitMaxPolls = 1u << 26;
 constexpr int32_t ZERO_DEVERR_WAIT_TIMEOUT = 1;
+// While unwinding after ZERO_DEVERR_WAIT_TIMEOUT, a CTA waits up to
+// kDrainTries bounded waits for each of its loads still in flight; one that
+// never lands is reported with this bit.
+constexpr int32_t ZERO_DEVERR_DRAIN_TIMEOUT = 2;
+constexpr int kDrainTries = 4;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

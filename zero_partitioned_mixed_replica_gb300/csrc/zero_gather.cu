@@ -37,9 +37,85 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
     }
 }
 
+struct CastArgs {
+    const float* master[kMaxRanks];
+    uint16_t* out[kMaxRanks];
+    uint32_t shard_v;  // per-rank shard length / 8
+    uint32_t total_v;  // nd * shard_v
+    int32_t nd;
+};
+
+// Round-to-nearest-even cast of every rank's fp32 master shard to 16 bits,
+// written the way the update's epilogue writes it: ZeRO-1/2 full replicas
+// receive rank r's shard at its flat position in every replica (cast +
+// all-gather, "第 5 课" §3 steps 2-3); shard outputs receive it in the rank's
+// own 16-bit shard (ZeRO-3).
+template <int ND, class F, int OUT>
+__global__ void __launch_bounds__(kThreads) cast_kernel(const __grid_constant__ CastArgs a) {
+    const int nd = ND > 0 ? ND : a.nd;
+    for (uint32_t v = blockIdx.x * kThreads + threadIdx.x; v < a.total_v; v += gridDim.x * kThreads) {
+        const uint32_t r = v / a.shard_v;
+        const size_t o = (size_t)(v - r * a.shard_v) * kVec;
+        float p[8];
+        ld8(a.master[r] + o, p);
+        const uint4 h = pack8<F>(p);
+        if constexpr (OUT == ZERO_OUT_FULL_REPLICAS) {
+            const size_t fo = (size_t)v * kVec;  // ZeRO-1/2: rank-major shard order is flat order
+            if constexpr (ND > 0) {
+#pragma unroll
+                for (int q = 0; q < ND; ++q) st_stream(a.out[q] + fo, h);
+            } else {
+                for (int q = 0; q < nd; ++q) st_stream(a.out[q] + fo, h);
+            }
+        } else {
+            st_stream(a.out[r] + o, h);
+        }
+    }
+}
+
 }  // namespace zk
 
 using namespace zero_detail;
+
+template <int ND, class F>
+static zero_status_t launch_cast(const zk::CastArgs& a, int32_t out_kind, cudaStream_t s) {
+    const int64_t work = ((int64_t)a.total_v + zk::kThreads - 1) / zk::kThreads;
+    if (out_kind == ZERO_OUT_FULL_REPLICAS) {
+        auto kern = zk::cast_kernel<ND, F, ZERO_OUT_FULL_REPLICAS>;
+        kern<<<persistent_grid(kern, work), zk::kThreads, 0, s>>>(a);
+    } else {
+        auto kern = zk::cast_kernel<ND, F, ZERO_OUT_SHARDS>;
+        kern<<<persistent_grid(kern, work), zk::kThreads, 0, s>>>(a);
+    }
+    return after_launch("zero_cast_params");
+}
+
+extern "C" zero_status_t zero_cast_params(const zero_layout* L, const float* const* master,
+                                          void* const* param16_out, int32_t out_kind, zero_stream_t stream) {
+    clear_error();
+    if (!L) return fail(ZERO_ERR_INVALID, "zero_cast_params: NULL layout");
+    if (L->stage == 0) return fail(ZERO_ERR_STATE, "zero_cast_params: stage 0 has no partitioned state");
+    if (out_kind != ZERO_OUT_FULL_REPLICAS && out_kind != ZERO_OUT_SHARDS)
+        return fail(ZERO_ERR_INVALID, "zero_cast_params: unknown out_kind");
+    if (L->stage == 3 && out_kind != ZERO_OUT_SHARDS)
+        return fail(ZERO_ERR_STATE, "zero_cast_params: ZeRO-3 writes 16-bit shards only");
+    zero_status_t rc;
+    if ((rc = check_ptr_array((const void* const*)master, L->n_d, "zero_cast_params master")) != ZERO_OK) return rc;
+    if ((rc = check_ptr_array((const void* const*)param16_out, L->n_d, "zero_cast_params param16_out")) != ZERO_OK)
+        return rc;
+    zk::CastArgs a{};
+    for (int r = 0; r < L->n_d; ++r) {
+        a.master[r] = master[r];
+        a.out[r] = static_cast<uint16_t*>(param16_out[r]);
+    }
+    a.shard_v = (uint32_t)(L->shard_len / zk::kVec);
+    a.total_v = (uint32_t)((int64_t)L->n_d * (L->shard_len / zk::kVec));
+    a.nd = L->n_d;
+    if (a.total_v == 0) return ZERO_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ZK_DISPATCH(L->n_d, L->dtype, return launch_cast<ND, F>(a, out_kind, s));
+    return ZERO_OK;
+}
 
 // Resident CTAs per SM: at N_d = 2, launches long enough to give every thread
 // ~64 vectors at 6 CTAs per SM run faster with 6 than with all 8 that fit

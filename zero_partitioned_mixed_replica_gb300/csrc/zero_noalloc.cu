@@ -26,25 +26,62 @@ constexpr size_t kScratchBytes = kPartialBytes + (size_t)zero_detail::kNormBlock
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
+// Unique id of the calling thread's current CUDA context, through the
+// driver's cuCtxGetCurrent / cuCtxGetId reached by the runtime's entry-point
+// query (the library links no driver library).  False if there is no current
+// context yet or the query is unavailable.
+bool current_context_id(unsigned long long* id) {
+    typedef int (*get_current_fn)(void**);
+    typedef int (*get_id_fn)(void*, unsigned long long*);
+    static get_current_fn get_current = nullptr;
+    static get_id_fn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<get_current_fn>(f);
+        f = nullptr;
+        q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<get_id_fn>(f);
+    });
+    if (!get_current || !get_id) return false;
+    void* ctx = nullptr;
+    if (get_current(&ctx) != 0 || !ctx) return false;
+    return get_id(ctx, id) == 0;
+}
+
 // Device address of g_noalloc_scratch on the current device.  In host code
-// the symbol names a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// the symbol names a host-side stand-in, so the address is looked up with the
+// device current, at the first call on that device, and cached together with
+// the id of the context it belongs to.  A call under another context of the
+// same device (after cudaDeviceReset, or after the primary context was
+// released and created again) looks the address up again instead of using a
+// stale one.
 zero_status_t scratch_address(void** out) {
     static std::mutex mu;
     static void* addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return zero_detail::fail(ZERO_ERR_CUDA, std::string("zero_fused_step_noalloc: ") +
                                                                       cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return zero_detail::fail(ZERO_ERR_CUDA, "zero_fused_step_noalloc: device index >= 64");
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (!addr[dev] || !have_id || id != ctx_of[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return zero_detail::fail(ZERO_ERR_CUDA, std::string("zero_fused_step_noalloc: cudaGetSymbolAddress: ") +
                                                         cudaGetErrorString(e));
         addr[dev] = p;
+        // the lookup makes the device's primary context current if none was
+        ctx_of[dev] = current_context_id(&id) ? id : 0;
     }
     *out = addr[dev];
     return ZERO_OK;

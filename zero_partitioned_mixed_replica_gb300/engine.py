@@ -116,7 +116,8 @@ class ZeroStep:
 
     def set_bucket_elems(self, bucket_elems: int) -> None:
         """Re-lay the same buffers with another bucket size (ZeRO-1/2): the
-        padded length and shards do not depend on it, so nothing moves."""
+        padded length and shards do not depend on it, so nothing moves (the
+        step arguments stay valid)."""
         if self.stage == 3:
             raise ValueError("ZeRO-3 reduces per unit")
         L = B.zero_layout_init(self.numels, None, self.n_d, self.stage, self.pad_multiple, bucket_elems, self.dtype)
@@ -160,36 +161,53 @@ class ZeroStep:
     def load_master(self, flat_master: torch.Tensor) -> None:
         """Scatter a flat fp32 master (Psi_pad, zero padding) into the rank
         shards, zero m and v, and set the 16-bit parameters to its
-        round-to-nearest-even cast."""
+        round-to-nearest-even cast (the library's zero_cast_params: into the
+        16-bit shards and/or every full replica)."""
         if flat_master.numel() != self.info.psi_pad:
             raise ValueError("load_master needs Psi_pad = %d elements, got %d" % (self.info.psi_pad, flat_master.numel()))
-        fm = flat_master.to(self.device, torch.float32)
+        if flat_master.dtype != torch.float32:
+            raise ValueError("load_master takes the fp32 master, got %s" % flat_master.dtype)
+        fm = flat_master.to(self.device)
         for u in self.units:
             for r in range(self.n_d):
                 lo = u.offset + r * u.shard
                 self.master[r, u.shard_base:u.shard_base + u.shard].copy_(fm[lo:lo + u.shard])
         self.m.zero_()
         self.v.zero_()
-        p16 = fm.to(TORCH_16[self.dtype])
+        s = self._s()
         if self.shard16 is not None:
-            for u in self.units:
-                for r in range(self.n_d):
-                    lo = u.offset + r * u.shard
-                    self.shard16[r, u.shard_base:u.shard_base + u.shard].copy_(p16[lo:lo + u.shard])
+            B.zero_cast_params(self.L, self.master_rows, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
         if self.params is not None:
-            self.params.copy_(p16.unsqueeze(0).expand(self.n_d, -1))
+            B.zero_cast_params(self.L, self.master_rows, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, s)
 
     # -- the step ------------------------------------------------------------------
-    def step(self) -> None:
-        self._step(None, self.per_bucket)
+    def step_args(self) -> B.StepArgs:
+        """This engine's buffers and settings as the library's zero_step_args
+        (built once: the buffers never move)."""
+        if getattr(self, "_args", None) is None:
+            stage3 = self.stage == 3
+            self._args = B.StepArgs(
+                self.L, self.hp, self.max_norm if not self.fused else 0.0, self.fused, self.per_bucket,
+                self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
+                None if self.fused else self.gshard_rows, None if stage3 else self.param_rows,
+                self.shard16_rows if (stage3 or not self.fuse_allgather) else None,
+                self.transient_rows if stage3 else None, self.state, self.workspace)
+        return self._args
 
-    def _step(self, wait, per_bucket: bool) -> None:
-        """The step's call order.  ``wait(k)``, if given, is called before the
-        first call that reads the gradient replicas of bucket k (ZeRO-3: unit
-        k) and orders the step's stream after their arrival."""
+    def step(self) -> None:
+        """One step.  The library's step executor (zero_step) issues the
+        calls; with per-call timers or a transient hook set, the same calls
+        are issued from here instead, one by one."""
+        if self.timers is None and self.transient_hook is None:
+            B.zero_step(self.L, self.step_args(), self._s())
+        else:
+            self._step(self.per_bucket)
+
+    def _step(self, per_bucket: bool) -> None:
+        """The step's calls issued one by one, in zero_step's order, so that
+        each can be timed (``timers``) or followed by the transient hook."""
         s = self._s()
         L, C = self.L, self._call
-        ready = wait if wait is not None else (lambda k: None)
         if self.stage == 3:
             U = len(self.units)
             for u in range(U):                                   # forward
@@ -200,7 +218,6 @@ class ZeroStep:
                 C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
                 if self.transient_hook:
                     self.transient_hook("bwd", u, self.transient_rows)
-                ready(u)
                 if self.fused:
                     C("fused_step", B.zero_fused_step, L, u, self.hp, self.grad_rows, self.master_rows,
                       self.m_rows, self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
@@ -219,20 +236,16 @@ class ZeroStep:
         if self.fused:
             if per_bucket:
                 for b in reversed(range(self.n_buckets)):
-                    ready(b)
                     C("fused_step", B.zero_fused_step, L, b, self.hp, self.grad_rows, self.master_rows,
                       self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
                       self.workspace, s)
             else:
-                for b in reversed(range(self.n_buckets)):
-                    ready(b)
                 C("fused_step", B.zero_fused_step, L, -1, self.hp, self.grad_rows, self.master_rows,
                   self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
                   self.workspace, s)
             C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
         else:
             for b in reversed(range(self.n_buckets)):
-                ready(b)
                 C("reduce_scatter", B.zero_reduce_scatter, L, b, self.grad_rows, self.gshard_rows, self.state,
                   self.workspace, s)
             C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
@@ -376,49 +389,26 @@ class ZeroStep:
         if need_pinned and not host.is_pinned():
             raise ValueError("overlapped host copies need pinned host memory")
 
-    def step_from_host(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
-        """One step whose N_d gradient replicas come from pinned host memory.
-
-        Each bucket's range (ZeRO-3: each unit's) is copied on two copy
-        streams in the order the step consumes them, and each reduce-scatter
-        or fused update waits only for its own range.  So later buckets cross
-        the host link while earlier ones are reduced.  This is the bucketed
-        overlap of "ZeRO: Memory Optimizations Toward Training Trillion
-        Parameter Models" reading notes §4.1-§4.2 (a bucket's reduce-scatter
-        starts as soon as backward has filled it, while the next is being
-        produced), with the host link standing in for backward.  Fused steps
-        run per bucket here.
-        The result is identical to ``upload_grads(host)`` then ``step()``."""
+    def step_from_host(self, host: torch.Tensor, chunk_elems: int = 1 << 27,
+                       state_out: Optional[torch.Tensor] = None) -> None:
+        """One step whose N_d gradient replicas come from pinned host memory,
+        through the library's zero_step_from_host: each bucket's range
+        (ZeRO-3: each unit's) is copied on the library's two copy streams in
+        the order the step consumes them, and each bucket's reduce-scatter or
+        fused update waits only for its own range, so later buckets cross the
+        host link while earlier ones are reduced (reading notes "ZeRO: Memory
+        Optimizations Toward Training Trillion Parameter Models" §4.1-§4.2: a
+        bucket is reduced as soon as backward has filled it; the host link
+        stands in for backward).  ``state_out`` (96 bytes of host memory,
+        pinned for an asynchronous copy) receives the step state at the end
+        of the step.  The result is identical to ``upload_grads(host)`` then
+        ``step()``."""
         self._check_host(host, True)
-        if getattr(self, "_copy_streams", None) is None:
-            self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
-        cur = self._s()
-        for cs in self._copy_streams:           # the previous step has finished reading the replicas
-            cs.wait_stream(cur)
-        if self.stage == 3:
-            order = [(u, self.units[u].offset, self.units[u].offset + self.units[u].padded)
-                     for u in reversed(range(len(self.units)))]
-        else:
-            order = [(b,) + tuple(B.zero_layout_bucket(self.L, b)) for b in reversed(range(self.n_buckets))]
-        events, i = {}, 0
-        for k, lo, hi in order:
-            for r in range(self.n_d):
-                for off in range(lo, hi, chunk_elems):
-                    end = min(hi, off + chunk_elems)
-                    with torch.cuda.stream(self._copy_streams[i % 2]):
-                        self.grads[r, off:end].copy_(host[r, off:end], non_blocking=True)
-                    i += 1
-            events[k] = []
-            for cs in self._copy_streams:
-                ev = torch.cuda.Event()
-                ev.record(cs)
-                events[k].append(ev)
-
-        def wait(k):
-            for ev in events[k]:
-                cur.wait_event(ev)
-
-        self._step(wait, True)
+        if state_out is not None and (state_out.device.type != "cpu" or state_out.numel() * state_out.element_size()
+                                      < self.state.numel()):
+            raise ValueError("state_out must be a host tensor of at least 96 bytes")
+        B.zero_step_from_host(self.L, self.step_args(), [host[r] for r in range(self.n_d)], chunk_elems,
+                              state_out, self._s())
 
     def upload_grads(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
         """Copy the N_d gradient replicas from (pinned) host memory, in chunks
