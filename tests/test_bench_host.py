@@ -55,8 +55,11 @@ def _run(args, env_extra=None):
 
 
 def test_reference_arm_json_line():
+    import time
+    t0 = time.perf_counter()
     p = _run(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1",
               "--cpu-seconds", "0.5"])
+    wall = time.perf_counter() - t0
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -69,6 +72,27 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+    # every step is the whole workload and ms_per_step is measured: K steps fit in the run's wall time
+    assert d["ms_per_step"] * d["steps"] / 1e3 <= wall
+    assert "sample" not in d["config"] and "the whole layout" in d["cpu_baseline"]["sample"]
+    assert d["value"] == pytest.approx(d["config"]["psi"] / (d["ms_per_step"] / 1e3), rel=1e-9)
+
+
+def test_oracle_samples_are_whole_tensors_of_the_workload():
+    import bench
+    from zero_partitioned_mixed_replica_gb300 import synth, workloads
+    w = workloads.gpt2_xl()
+    numels, units, scales, desc = bench.oracle_sample(w, 2)
+    assert len(numels) == 24 and units == [0] * 12 + [1] * 12
+    assert numels == w.numels[2:26]                          # block 1 and block 2, after wte and wpe
+    assert scales == synth.tensor_scales(len(w.numels))[2:26]  # each tensor keeps its own scale
+    full = bench.oracle_sample(w, None)
+    assert full[0] == w.numels and "whole layout" in full[3]
+    gb = 10 ** 9
+    assert bench.oracle_blocks_that_fit(w, 199 * gb) is None      # the 1.5B oracle state fits a 199 GB host
+    k = bench.oracle_blocks_that_fit(w, 62 * gb)
+    assert 1 <= k < 48
+    assert bench.oracle_bytes(w, sum(bench.oracle_sample(w, k)[0])) <= 0.6 * 62 * gb
 
 
 def test_reference_arm_nonzero_rank_exits_quietly():
