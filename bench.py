@@ -13,17 +13,20 @@ step decision -> sharded AdamW with the all-gather fused in.
                   [--workload gpt2_xl|gpt2_small|llama7b|gpt2_medium|tiny|gpt2_xl_block|llama7b_block]
                   [--graph] [--whole-buffer] [--micro M] [--sweep] [--prefetch] [--checkpoint DIR]
 
-The e2e value repeats the step with the gradient replicas copied every step
-from pinned host memory (ZeroStep.step_from_host: per-bucket copies overlapped
-with the reduce-scatter) and the step state read back, after untimed warm-up
-steps; it reports the host link's rate and the copies' time beside it.
+The e2e value repeats the step through the library's host-buffer entry point
+(zero_step_from_host, one C-ABI call per step): the gradient replicas are
+copied every step from pinned host memory, per bucket, overlapped with the
+reduce-scatter, and the step state is copied back to host memory, after
+untimed warm-up steps; it reports the host link's rate and the copies' time
+beside it.
 
 Under torchrun (N > 1) every rank runs its own independent replica of the
 step on its own GPU (the simulated ranks live inside one GPU; there is no
 data-path collective); a gloo barrier brackets the timed region and rank 0
 prints the max-over-ranks time.  ``--impl reference`` times the CPU oracle on
-the host cores instead (rank 0 only), on a bounded sample of the same
-workload.  One JSON line is printed by rank 0.
+the host cores instead (rank 0 only): exactly W untimed and K timed steps over
+the whole workload, each step's wall time measured.  One JSON line is printed
+by rank 0.
 """
 from __future__ import annotations
 
@@ -54,7 +57,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="gpt2_xl")
     p.add_argument("--e2e-steps", type=int, default=5)
-    p.add_argument("--cpu-sample", type=int, default=0, help="oracle sample size in parameters")
+    p.add_argument("--cpu-blocks", type=int, default=0,
+                   help="oracle timing on the workload's first N transformer blocks (0: the cpu_baseline "
+                        "takes about 10-30 s of blocks; the reference arm takes the whole layout if it fits)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
@@ -267,41 +272,85 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_timing(w, sample_params: int, min_seconds: float, min_steps: int = 3, max_steps: int = 10 ** 6,
-                  warmup: int = 1):
-    """The oracle's step on a bounded sample of the workload: ``warmup``
-    untimed steps, then at least ``min_steps`` timed steps and at least
-    ``min_seconds`` of them (at most ``max_steps``)."""
-    import numpy as np
+def oracle_sample(w, blocks):
+    """The tensors of the workload that the oracle is timed on: all of them
+    (``blocks`` None), or those of its first ``blocks`` transformer blocks
+    (ZeRO-3 units 1..blocks), each with its own per-tensor scale.  Returns
+    (numels, unit ids, scales, description)."""
+    from zero_partitioned_mixed_replica_gb300 import synth
+    scales_all = synth.tensor_scales(len(w.numels)) if w.per_tensor_scale else None
+    n_blocks = max(w.unit_of_tensor)
+    if blocks is None or blocks >= n_blocks:
+        return (list(w.numels), list(w.unit_of_tensor), scales_all,
+                "the whole layout: %d tensors, Psi = %d" % (len(w.numels), w.psi))
+    keep = [t for t, u in enumerate(w.unit_of_tensor) if 1 <= u <= blocks]
+    numels = [w.numels[t] for t in keep]
+    units = [w.unit_of_tensor[t] - 1 for t in keep]
+    scales = [scales_all[t] for t in keep] if scales_all is not None else None
+    return (numels, units, scales,
+            "the first %d of %d transformer blocks (%d tensors, %d parameters, %.2f%% of Psi)"
+            % (blocks, n_blocks, len(numels), sum(numels), 100.0 * sum(numels) / w.psi))
+
+
+def oracle_bytes(w, psi: int) -> int:
+    """Host bytes the oracle's ZeRO simulation holds for ``psi`` parameters:
+    the N_d 16-bit gradient replicas, fp32 master/m/v/reduced shards, the
+    16-bit parameters (full replicas for ZeRO-1/2) and the initial master."""
+    p16 = 2 * w.n_d if w.stage != 3 else 2
+    return int(psi * (2 * w.n_d + 16 + p16 + 4) * 1.1)
+
+
+def oracle_blocks_that_fit(w, avail) -> object:
+    """None (the whole layout) if its oracle state takes at most 60% of the
+    host's available memory, else the most leading blocks that do."""
+    if avail is None or oracle_bytes(w, w.psi) <= 0.6 * avail:
+        return None
+    per_block = max(1, sum(n for n, u in zip(w.numels, w.unit_of_tensor) if u == 1))
+    return max(1, int(0.6 * avail // oracle_bytes(w, per_block)))
+
+
+def oracle_timing(w, blocks, min_seconds: float, min_steps: int = 3, max_steps: int = 10 ** 6, warmup: int = 1):
+    """The oracle (its literal ZeRO simulation, as it stands) on the
+    workload's tensors (see :func:`oracle_sample`) with the workload's
+    settings: N_d, stage, bucket size, 16-bit format, per-tensor scales, loss
+    scale, clipping.  ``warmup`` untimed steps, then at least ``min_steps``
+    timed steps and at least ``min_seconds`` of them (at most ``max_steps``).
+    Each step's wall time is measured; nothing is extrapolated."""
     from oracle.layout import make_layout
     from oracle.step import AdamWHP, ZeroSimulation, num_threads
     from zero_partitioned_mixed_replica_gb300 import synth
 
-    numels = [sample_params]
-    units = [0] if w.stage == 3 else None
+    numels, units, scales, desc = oracle_sample(w, blocks)
     L = make_layout(numels, w.n_d, w.stage, bucket_elems=w.bucket_elems if w.stage != 3 else 0,
-                    unit_of_tensor=units)
+                    unit_of_tensor=units if w.stage == 3 else None)
     m0 = synth.master_init(numels, L.tensor_offsets, L.psi_pad, w.master_std).numpy()
     reps = [synth.as_u16(synth.grad_replica(numels, L.tensor_offsets, L.psi_pad, w.dtype, r, 1, w.grad_std,
-                                            None, w.loss_scale)) for r in range(w.n_d)]
+                                            scales, w.loss_scale)) for r in range(w.n_d)]
     zs = ZeroSimulation(L, m0, w.dtype, AdamWHP(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay),
                         max_norm=w.max_norm, loss_scale=w.loss_scale, dynamic=w.dynamic_scale,
                         growth_interval=w.growth_interval)
+    del m0
     for _ in range(warmup):                         # untimed warm-up steps
         zs.step(reps)
-    n, t0 = 0, time.perf_counter()
-    while n < max_steps and (n < min_steps or time.perf_counter() - t0 < min_seconds):
+    times = []
+    t0 = time.perf_counter()
+    while len(times) < max_steps and (len(times) < min_steps or time.perf_counter() - t0 < min_seconds):
+        a = time.perf_counter()
         zs.step(reps)
-        n += 1
-    dt = (time.perf_counter() - t0) / n
-    return {"value": sample_params / dt, "unit": "params/s", "cores": num_threads(), "kind": "oracle",
-            "sample": "%d parameters (%.3f%% of the workload), N_d=%d, stage %d, %d timed steps of %.3f s"
-                      % (sample_params, 100.0 * sample_params / w.psi, w.n_d, w.stage, n, dt),
-            "s_per_step": dt, "steps": n}
+        times.append(time.perf_counter() - a)
+    dt = sum(times) / len(times)
+    psi = sum(numels)
+    return {"value": psi / dt, "unit": "params/s", "cores": num_threads(), "kind": "oracle",
+            "sample": "%s; N_d=%d, stage %d, %s grads, %d untimed + %d timed steps of %.3f s (measured, mean)"
+                      % (desc, w.n_d, w.stage, "fp16" if w.dtype == 1 else "bf16", warmup, len(times), dt),
+            "s_per_step": dt, "steps": len(times), "psi": psi}
 
 
-def default_sample(w) -> int:
-    return min(w.psi, max(1 << 20, 16_000_000 if w.n_d <= 8 else 4_000_000))
+def default_cpu_blocks(w) -> int:
+    """Leading blocks for the repo arm's cpu_baseline: about 10-30 s of CPU
+    work on the machine's cores (a GPT-2 1.5B block is 30.7M parameters)."""
+    per_block = sum(n for n, u in zip(w.numels, w.unit_of_tensor) if u == 1)
+    return max(1, min(max(w.unit_of_tensor), int(120_000_000 // max(1, per_block))))
 
 
 # ---------------------------------------------------------------------------
@@ -354,8 +403,15 @@ def gpu_run(args, w, rank, world, local_rank):
         uuid = None
     clocks = ClockSampler(uuid)
     time.sleep(0.3)
-    if graph is None:
+    # per-call durations from CUDA events on each call's launching stream: the library's
+    # launch tracing for the step executor (zero_step); the engine's own per-call events
+    # for the micro-batch calls it issues itself
+    trace = graph is None and args.micro == 1
+    if graph is None and args.micro > 1:
         eng.timers = {}
+    if trace:
+        B.zero_trace_read(reset=True)
+        B.zero_trace_enable(True)
     B.zero_launch_count(reset=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -369,6 +425,10 @@ def gpu_run(args, w, rank, world, local_rank):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     timers, eng.timers = eng.timers, None
+    traced = None
+    if trace:
+        B.zero_trace_enable(False)
+        traced = B.zero_trace_read(reset=True)
     ms = max_over_ranks(ms, world)
     if graph is not None:
         # launches inside a replayed graph are the captured ones
@@ -380,7 +440,9 @@ def gpu_run(args, w, rank, world, local_rank):
 
     # --- per-kernel averages from events on the launching stream ------------------
     kern = {}
-    if timers:
+    if traced:
+        kern = traced
+    elif timers:
         for name, evs in timers.items():
             d = [a.elapsed_time(b) for a, b in evs]
             kern[name] = {"launches": len(d), "total_ms": sum(d), "avg_ms": sum(d) / len(d)}
@@ -404,12 +466,14 @@ def gpu_run(args, w, rank, world, local_rank):
 
             def e2e_step():
                 if args.micro == 1:
-                    eng.step_from_host(host_grads)     # per-bucket copies overlap the reduce-scatter
+                    # one C-ABI call (zero_step_from_host): the per-bucket host-to-device copies
+                    # overlap the reduce-scatter, and the step state is copied back to host_state
+                    eng.step_from_host(host_grads, state_out=host_state)
                 else:
                     for mb in range(args.micro):
                         eng.upload_grads(host_grads)
                         eng.micro_step(mb)
-                host_state.copy_(eng.state, non_blocking=True)
+                    host_state.copy_(eng.state, non_blocking=True)
 
             # Untimed warm-up, as for the device-resident steps: the first
             # whole-buffer passes over a freshly pinned buffer cross the host
@@ -624,18 +688,21 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        sample = args.cpu_sample or default_sample(w)
-        # exactly W untimed and K timed oracle steps, each on the bounded sample
-        cb = oracle_timing(w, sample, min_seconds=0.0, min_steps=max(1, args.steps), max_steps=max(1, args.steps),
+        # the oracle on the host cores, exactly W untimed and K timed steps over the whole
+        # workload (or, where its state would not fit the host's memory, named leading blocks)
+        blocks = args.cpu_blocks if args.cpu_blocks > 0 else oracle_blocks_that_fit(w, host_mem_available())
+        cb = oracle_timing(w, blocks, min_seconds=0.0, min_steps=max(1, args.steps), max_steps=max(1, args.steps),
                            warmup=max(0, args.warmup))
         line = {"metric": METRIC, "value": cb["value"], "unit": "params/s", "impl": "reference",
                 "n_gpus": args.gpus, "steps": cb["steps"], "warmup": max(0, args.warmup),
-                "ms_per_step": cb["s_per_step"] * 1e3 * w.psi / sample,
+                "ms_per_step": cb["s_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic", "config": workload_desc,
                 "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
                 "e2e": {"value": cb["value"], "unit": "params/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
+        if cb["psi"] != w.psi:
+            line["config"] = dict(workload_desc, sample=cb["sample"].split(";")[0], sample_psi=cb["psi"])
         print(json.dumps(line), flush=True)
         return
 
@@ -665,8 +732,8 @@ def main():
             roof["achieved_by_ncu_bytes"] = roof["traffic"] / (kern[dom]["avg_ms"] / 1e3) / 1e9
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:   # the oracle baseline: rank 0 at N = 1 only
-        sample = args.cpu_sample or default_sample(w)
-        cb = oracle_timing(w, sample, min_seconds=args.cpu_seconds)
+        blocks = args.cpu_blocks if args.cpu_blocks > 0 else default_cpu_blocks(w)
+        cb = oracle_timing(w, blocks, min_seconds=args.cpu_seconds)
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         cpu["gbs"] = cb["value"] * bpp / 1e9     # the host's rate in the step's algorithmic bytes
     if rank != 0:

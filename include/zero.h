@@ -376,11 +376,17 @@ typedef struct zero_step_args {
  *     u = U-1..0: gather u again and zero_fused_step(u) (fused) or
  *     zero_reduce_scatter(u) (split, followed by the norm and the shard
  *     update after the loop).
- * Asynchronous on `stream`; allocates nothing; captures into a CUDA graph
- * like the calls it issues.  Errors: those of the calls it issues (the first
- * failing call stops the step and its status is returned); inconsistent
- * arguments (fused with max_norm > 0, missing buffers for the stage) give
- * ZERO_ERR_INVALID before any launch. */
+ * ZeRO-1/2 bucket launches alternate between `stream` and a second stream of
+ * the library's (one per device, created at the first call), which joins
+ * `stream` again before the norm: consecutive buckets touch disjoint elements
+ * and norm-partial slots, so one bucket's launch can start while the previous
+ * one drains.  Results do not depend on it.
+ * Asynchronous on `stream`; allocates no device memory; captures into a CUDA
+ * graph like the calls it issues.  Calls on one device are serialised by a
+ * library lock.  Errors: those of the calls it issues (the first failing call
+ * stops the step and its status is returned); inconsistent arguments (fused
+ * with max_norm > 0, missing buffers for the stage) give ZERO_ERR_INVALID
+ * before any launch. */
 zero_status_t zero_step(const zero_layout* L, const zero_step_args* args, zero_stream_t stream);
 
 /* zero_step with the N_d gradient replicas in host memory.  host_grads: N_d
@@ -403,6 +409,37 @@ zero_status_t zero_step(const zero_layout* L, const zero_step_args* args, zero_s
 zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* args,
                                   const void* const* host_grads, int64_t chunk_elems, void* host_state,
                                   zero_stream_t stream);
+
+/* Launch tracing of zero_step and zero_step_from_host.  With tracing on,
+ * every library call the executor issues is bracketed by two timing events
+ * recorded on the stream the call is issued on (none while that stream is
+ * being captured into a CUDA graph); zero_trace_read waits for the recorded
+ * events and adds up the elapsed time per kind of call. */
+enum {
+    ZERO_CALL_REDUCE_SCATTER = 0,
+    ZERO_CALL_GRAD_NORM = 1,      /* both passes of zero_grad_norm */
+    ZERO_CALL_ADAMW = 2,
+    ZERO_CALL_FUSED_STEP = 3,
+    ZERO_CALL_STAGE3_GATHER = 4,
+    ZERO_CALL_ALLGATHER = 5,
+    ZERO_CALL_KINDS = 6
+};
+typedef struct zero_trace_totals {
+    int64_t calls[8];             /* traced calls per ZERO_CALL_* kind          */
+    double total_ms[8];           /* sum of their event-timed durations (ms)    */
+    double busy_ms[8];            /* time with at least one of them in flight:
+                                     equals total_ms unless calls of the kind
+                                     overlapped (alternating bucket streams)   */
+} zero_trace_totals;
+
+/* Turn tracing on (1) or off (0), process-wide; returns the previous setting. */
+int32_t zero_trace_enable(int32_t on);
+
+/* Totals of the calls traced since the last reset.  Blocks until every
+ * recorded event has completed.  reset != 0 clears the record afterwards (its
+ * events are reused).  Errors: NULL out (ZERO_ERR_INVALID); a failing event
+ * query (ZERO_ERR_CUDA). */
+zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset);
 
 /* ------------------------------------------------------------------------ */
 /* Gradient accumulation over M micro-batches per optimizer step             */

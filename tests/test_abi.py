@@ -200,11 +200,15 @@ def test_executor_and_cast_validate_before_launch():
     assert status(B.zero_step, L3, args(L3, True, full=None, shards=two), 0) == B.ZERO_ERR_INVALID  # no transient
     assert status(B.zero_step, L3, args(L3, True, full=None, transient=two), 0) == B.ZERO_ERR_INVALID  # no shards
     assert status(B.zero_step, L0, args(L0, False), 0) == B.ZERO_ERR_STATE
-    # the first call the executor issues validates its own pointers before launching
+    # every pointer is validated before the executor touches the device
     assert status(B.zero_step, L, args(L, False, grads=[FAKE, MIS]), 0) == B.ZERO_ERR_ALIGN
+    assert status(B.zero_step, L, args(L, False, gshard=[0, FAKE]), 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_step_from_host, L, args(L, False), None, 0, None, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_step_from_host, L, args(L, False), [FAKE, 0], 0, None, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_step_from_host, L, args(L, True, max_norm=0.5), two, 0, None, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_step_from_host, L, args(L, False, full=[FAKE, MIS]), two, 0, None, 0) == B.ZERO_ERR_ALIGN
+    assert B.lib().zero_trace_read(None, 0) == B.ZERO_ERR_INVALID
+    assert B.zero_trace_read() == {}             # nothing traced: no kind reported
     assert status(B.zero_cast_params, L3, two, two, B.ZERO_OUT_FULL_REPLICAS, 0) == B.ZERO_ERR_STATE
     assert status(B.zero_cast_params, L, two, two, 5, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_cast_params, L, [FAKE, MIS], two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_ALIGN

@@ -455,3 +455,35 @@ def test_native_executor_equals_call_by_call(mode):
     assert torch.equal(a.shard16, b.shard16) if z3 else torch.equal(a.params, b.params)
     if mode == "z2_split_clip_fp16":
         assert a.read_state()["skipped"] == 1
+
+
+def test_launch_tracing_counts_every_call_of_the_executor():
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    L = c.layout()
+    eng = _engine(c)
+    eng.load_master(torch.from_numpy(c.master0(L)))
+    for r, g in enumerate(c.grads_torch(L, 1, 1.0)):
+        eng.grads[r].copy_(g.cuda())
+    Bd.zero_trace_read(reset=True)
+    prev = Bd.zero_trace_enable(True)
+    try:
+        for _ in range(3):
+            eng.step()
+    finally:
+        Bd.zero_trace_enable(prev)
+    t = Bd.zero_trace_read(reset=True)
+    assert t["reduce_scatter"]["launches"] == 3 * eng.n_buckets
+    assert t["grad_norm"]["launches"] == 3 and t["adamw"]["launches"] == 3
+    for k in t.values():
+        assert 0 < k["busy_ms"] <= k["total_ms"] * (1 + 1e-6)
+    eng.step()                                   # tracing off: nothing recorded
+    assert Bd.zero_trace_read(reset=True) == {}
+    f = _engine(Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768))
+    Bd.zero_trace_enable(True)
+    try:
+        f.step()
+    finally:
+        Bd.zero_trace_enable(False)
+    t = Bd.zero_trace_read(reset=True)
+    assert t["fused_step"]["launches"] == f.n_buckets and t["grad_norm"]["launches"] == 1

@@ -39,7 +39,7 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_allgather_params", "zero_cast_params", "zero_stage3_gather_layer", "zero_fused_step",
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
             "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_step_from_host",
-            "zero_set_max_ctas",
+            "zero_trace_enable", "zero_trace_read", "zero_set_max_ctas",
             "zero_last_error", "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
@@ -80,6 +80,13 @@ class zero_copy_segment(ctypes.Structure):
 
 class zero_adamw_hp(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+ZERO_CALL_NAMES = ["reduce_scatter", "grad_norm", "adamw", "fused_step", "stage3_gather", "allgather"]
+
+
+class zero_trace_totals(ctypes.Structure):
+    _fields_ = [("calls", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8), ("busy_ms", ctypes.c_double * 8)]
 
 
 class zero_step_args(ctypes.Structure):
@@ -147,6 +154,7 @@ def lib():
         "zero_reduce_scatter_micro": [P, i32, i32, i32, PP, PP, P, P, P],
         "zero_step": [P, ctypes.POINTER(zero_step_args), P],
         "zero_step_from_host": [P, ctypes.POINTER(zero_step_args), PP, i64, P, P],
+        "zero_trace_read": [ctypes.POINTER(zero_trace_totals), i32],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -158,6 +166,8 @@ def lib():
     L.zero_last_error.restype = ctypes.c_char_p
     L.zero_launch_count.argtypes = [i32]
     L.zero_launch_count.restype = i64
+    L.zero_trace_enable.argtypes = [i32]
+    L.zero_trace_enable.restype = i32
     L.zero_set_max_ctas.argtypes = [i32]
     L.zero_set_max_ctas.restype = i32
     _lib = L
@@ -343,6 +353,22 @@ def zero_step_from_host(L: Layout, args: StepArgs, host_grads, chunk_elems: int 
     CPU tensor / address of 96 bytes, or None."""
     _check(lib().zero_step_from_host(L, ctypes.byref(args.args), _ptrs(host_grads, L), int(chunk_elems),
                                      _addr(host_state), _stream(stream)))
+
+
+def zero_trace_enable(on: bool) -> bool:
+    return bool(lib().zero_trace_enable(int(bool(on))))
+
+
+def zero_trace_read(reset: bool = True) -> dict:
+    """{call name: {"launches": n, "total_ms": t, "busy_ms": b, "avg_ms": b / n}}
+    for every kind of call traced since the last reset.  ``busy_ms`` is the
+    time with at least one call of the kind in flight; ``avg_ms`` divides it
+    by the calls (equal to total / n when no two calls of the kind overlapped)."""
+    t = zero_trace_totals()
+    _check(lib().zero_trace_read(ctypes.byref(t), int(bool(reset))))
+    return {name: {"launches": int(t.calls[k]), "total_ms": float(t.total_ms[k]), "busy_ms": float(t.busy_ms[k]),
+                   "avg_ms": float(t.busy_ms[k]) / int(t.calls[k])}
+            for k, name in enumerate(ZERO_CALL_NAMES) if t.calls[k] > 0}
 
 
 def zero_set_max_ctas(n: int) -> int:

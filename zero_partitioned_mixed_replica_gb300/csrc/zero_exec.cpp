@@ -22,6 +22,9 @@
 // host link standing in for backward.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
 #include <functional>
 #include <mutex>
 #include <string>
@@ -35,6 +38,16 @@ namespace {
 
 zero_status_t cuda_fail(const char* what, cudaError_t e) {
     return fail(ZERO_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+zero_status_t check_ptrs(const void* const* arr, int n, const std::string& what) {
+    if (!arr) return ZERO_OK;  // presence is checked per stage
+    for (int i = 0; i < n; ++i) {
+        if (!arr[i]) return fail(ZERO_ERR_INVALID, what + ": NULL device pointer");
+        if (reinterpret_cast<uintptr_t>(arr[i]) & 255u)
+            return fail(ZERO_ERR_ALIGN, what + ": device pointer not 256-byte aligned");
+    }
+    return ZERO_OK;
 }
 
 zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const char* what) {
@@ -54,93 +67,235 @@ zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const ch
         if (a->fused && a->param16_shards)
             return fail(ZERO_ERR_INVALID, w + ": the fused step writes the full replicas (param16_shards must be NULL)");
     }
-    return ZERO_OK;
-}
-
-// The step's calls on `s`.  ready(k) runs before the first call that reads the
-// gradient replicas of bucket k (ZeRO-3: unit k).
-zero_status_t run_step(const zero_layout* L, const zero_step_args* a, zero_stream_t s,
-                       const std::function<zero_status_t(int32_t)>& ready) {
+    if (!a->hp) return fail(ZERO_ERR_INVALID, w + ": NULL hyperparameters");
+    if (!a->grad_replicas || !a->master || !a->m || !a->v)
+        return fail(ZERO_ERR_INVALID, w + ": NULL pointer array");
+    const int n = L->n_d;
     zero_status_t rc;
-    const int32_t nb = (int32_t)L->buckets.size();
-    if (L->stage == 3) {
-        const int32_t U = (int32_t)L->segs.size();
-        for (int32_t u = 0; u < U; ++u)  // forward
-            if ((rc = zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, s)) != ZERO_OK)
-                return rc;
-        for (int32_t u = U - 1; u >= 0; --u) {  // backward
-            if ((rc = zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, s)) != ZERO_OK)
-                return rc;
-            if ((rc = ready(u)) != ZERO_OK) return rc;
-            rc = a->fused ? zero_fused_step(L, u, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                            a->param16_shards, ZERO_OUT_SHARDS, a->workspace, s)
-                          : zero_reduce_scatter(L, u, a->grad_replicas, a->grad_shards, a->state, a->workspace, s);
-            if (rc != ZERO_OK) return rc;
-        }
-        if (a->fused) return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, s);
-        if ((rc = zero_grad_norm(L, a->max_norm, ZERO_NORM_DECIDE, a->state, a->workspace, s)) != ZERO_OK) return rc;
-        return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards, a->state,
-                                     a->param16_shards, ZERO_OUT_SHARDS, s);
-    }
-    if (a->fused) {
-        if (a->per_bucket) {
-            for (int32_t b = nb - 1; b >= 0; --b) {
-                if ((rc = ready(b)) != ZERO_OK) return rc;
-                if ((rc = zero_fused_step(L, b, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                          a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, s)) != ZERO_OK)
-                    return rc;
-            }
-        } else {
-            for (int32_t b = nb - 1; b >= 0; --b)
-                if ((rc = ready(b)) != ZERO_OK) return rc;
-            if ((rc = zero_fused_step(L, -1, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                      a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, s)) != ZERO_OK)
-                return rc;
-        }
-        return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, s);
-    }
-    for (int32_t b = nb - 1; b >= 0; --b) {
-        if ((rc = ready(b)) != ZERO_OK) return rc;
-        if ((rc = zero_reduce_scatter(L, b, a->grad_replicas, a->grad_shards, a->state, a->workspace, s)) != ZERO_OK)
-            return rc;
-    }
-    if ((rc = zero_grad_norm(L, a->max_norm, ZERO_NORM_DECIDE, a->state, a->workspace, s)) != ZERO_OK) return rc;
-    if (!a->param16_shards)
-        return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards, a->state,
-                                     a->param16_full, ZERO_OUT_FULL_REPLICAS, s);
-    if ((rc = zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards, a->state,
-                                    a->param16_shards, ZERO_OUT_SHARDS, s)) != ZERO_OK)
-        return rc;
-    return zero_allgather_params(L, (const void* const*)a->param16_shards, a->param16_full, s);
+    if ((rc = check_ptrs(a->grad_replicas, n, w + " grad_replicas")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->master, n, w + " master")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->m, n, w + " m")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->v, n, w + " v")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->grad_shards, n, w + " grad_shards")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->param16_full, n, w + " param16_full")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->param16_shards, n, w + " param16_shards")) != ZERO_OK) return rc;
+    if ((rc = check_ptrs((const void* const*)a->transient, n, w + " transient")) != ZERO_OK) return rc;
+    const void* one[2] = {a->state, a->workspace};
+    if (!a->state || !a->workspace) return fail(ZERO_ERR_INVALID, w + ": NULL state or workspace");
+    return check_ptrs(one, 2, w + " state/workspace");
 }
 
-// Library-owned copy streams and events of one device, created at the first
-// host-input step on it and kept until the process exits.
-struct CopyStreams {
+// ---------------------------------------------------------------------------
+// Launch tracing: with tracing on, every call the executor issues is
+// bracketed by two timing events recorded on the stream it is issued on
+// (not while that stream is being captured into a graph).
+// ---------------------------------------------------------------------------
+struct TraceRecord {
+    int32_t kind;
+    int32_t dev;
+    cudaEvent_t e0, e1;
+};
+std::mutex g_trace_mu;
+std::atomic<int32_t> g_trace_on{0};
+std::vector<TraceRecord> g_trace;
+std::vector<cudaEvent_t> g_trace_free[64];
+
+bool trace_take(int dev, cudaEvent_t* e) {
+    auto& pool = g_trace_free[dev];
+    if (!pool.empty()) {
+        *e = pool.back();
+        pool.pop_back();
+        return true;
+    }
+    return cudaEventCreate(e) == cudaSuccess;
+}
+
+template <class Call>
+zero_status_t traced(int32_t kind, cudaStream_t st, Call&& call) {
+    if (!g_trace_on.load(std::memory_order_relaxed)) return call();
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    int dev = 0;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone ||
+        cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return call();
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_trace_mu);
+        if (!trace_take(dev, &e0)) return call();
+        if (!trace_take(dev, &e1)) {
+            g_trace_free[dev].push_back(e0);
+            return call();
+        }
+    }
+    cudaEventRecord(e0, st);
+    const zero_status_t rc = call();
+    cudaEventRecord(e1, st);
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    g_trace.push_back({kind, dev, e0, e1});
+    return rc;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device resources of the executor, created at first use and kept until
+// the process exits: a second stream for alternating bucket launches with its
+// fork/join events, and the host-input copy streams with their events.  One
+// lock per device serialises the calls that use them.
+// ---------------------------------------------------------------------------
+struct DeviceRes {
+    std::mutex mu;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
     cudaStream_t cs[2] = {nullptr, nullptr};
     cudaEvent_t start = nullptr;
     std::vector<cudaEvent_t> ev;  // two per bucket: one per copy stream
 };
+DeviceRes g_res[64];
 
-std::mutex g_copy_mu;
-CopyStreams g_copy[64];
-
-zero_status_t copy_streams(int dev, size_t n_events, CopyStreams** out) {
-    CopyStreams& c = g_copy[dev];
-    cudaError_t e;
-    for (int i = 0; i < 2; ++i)
-        if (!c.cs[i] && (e = cudaStreamCreateWithFlags(&c.cs[i], cudaStreamNonBlocking)) != cudaSuccess)
-            return cuda_fail("zero_step_from_host: copy stream", e);
-    if (!c.start && (e = cudaEventCreateWithFlags(&c.start, cudaEventDisableTiming)) != cudaSuccess)
-        return cuda_fail("zero_step_from_host: event", e);
-    while (c.ev.size() < n_events) {
-        cudaEvent_t x = nullptr;
-        if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_fail("zero_step_from_host: event", e);
-        c.ev.push_back(x);
-    }
-    *out = &c;
+zero_status_t current_res(DeviceRes** out, const char* what) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(what, e);
+    if (dev < 0 || dev >= 64) return fail(ZERO_ERR_CUDA, std::string(what) + ": device index >= 64");
+    *out = &g_res[dev];
     return ZERO_OK;
+}
+
+zero_status_t make_stream(cudaStream_t* s, const char* what) {
+    if (*s) return ZERO_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(what, e);
+}
+
+zero_status_t make_event(cudaEvent_t* ev, const char* what) {
+    if (*ev) return ZERO_OK;
+    cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(what, e);
+}
+
+zero_status_t step_res(DeviceRes& R, const char* what) {
+    zero_status_t rc;
+    if ((rc = make_stream(&R.aux, what)) != ZERO_OK) return rc;
+    if ((rc = make_event(&R.fork, what)) != ZERO_OK) return rc;
+    return make_event(&R.join, what);
+}
+
+zero_status_t wait_on(cudaStream_t waiter, cudaEvent_t ev, cudaStream_t recorder, const char* what) {
+    cudaError_t e = cudaEventRecord(ev, recorder);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(what, e);
+}
+
+using Ready = std::function<zero_status_t(int32_t, cudaStream_t)>;
+
+// Mean bucket length up to which consecutive bucket launches alternate
+// between two streams.
+constexpr int64_t kAlternateMaxElems = (int64_t)1 << 25;
+
+// The step's calls on `s`.  ready(k, stream) runs before the first call that
+// reads the gradient replicas of bucket k (ZeRO-3: unit k), on the stream
+// that call is issued on.
+//
+// Consecutive bucket launches of ZeRO-1/2 touch disjoint elements and write
+// their norm partials to fixed, disjoint slots, so short ones alternate
+// between `s` and the device's second stream: the next bucket's CTAs start on
+// the SMs that the previous bucket's last CTAs free, instead of after its
+// whole grid has drained.  The second stream joins `s` before the global
+// norm.  Results do not depend on it (every output element and partial has
+// one writer).  ZeRO-3 units share one transient buffer and stay on `s`.
+zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
+                       const Ready& ready) {
+    zero_status_t rc;
+    const int32_t nb = (int32_t)L->buckets.size();
+    const zero_stream_t zs = reinterpret_cast<zero_stream_t>(s);
+    if (L->stage == 3) {
+        const int32_t U = (int32_t)L->segs.size();
+        for (int32_t u = 0; u < U; ++u)  // forward
+            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, s, [&] {
+                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, zs);
+                 })) != ZERO_OK)
+                return rc;
+        for (int32_t u = U - 1; u >= 0; --u) {  // backward
+            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, s, [&] {
+                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, zs);
+                 })) != ZERO_OK)
+                return rc;
+            if ((rc = ready(u, s)) != ZERO_OK) return rc;
+            if (a->fused)
+                rc = traced(ZERO_CALL_FUSED_STEP, s, [&] {
+                    return zero_fused_step(L, u, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
+                                           a->param16_shards, ZERO_OUT_SHARDS, a->workspace, zs);
+                });
+            else
+                rc = traced(ZERO_CALL_REDUCE_SCATTER, s, [&] {
+                    return zero_reduce_scatter(L, u, a->grad_replicas, a->grad_shards, a->state, a->workspace, zs);
+                });
+            if (rc != ZERO_OK) return rc;
+        }
+        if (a->fused)
+            return traced(ZERO_CALL_GRAD_NORM, s, [&] {
+                return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, zs);
+            });
+        if ((rc = traced(ZERO_CALL_GRAD_NORM, s, [&] {
+                 return zero_grad_norm(L, a->max_norm, ZERO_NORM_DECIDE, a->state, a->workspace, zs);
+             })) != ZERO_OK)
+            return rc;
+        return traced(ZERO_CALL_ADAMW, s, [&] {
+            return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards,
+                                         a->state, a->param16_shards, ZERO_OUT_SHARDS, zs);
+        });
+    }
+    const bool one_launch = a->fused && !a->per_bucket;
+    if (one_launch) {
+        for (int32_t b = nb - 1; b >= 0; --b)
+            if ((rc = ready(b, s)) != ZERO_OK) return rc;
+        if ((rc = traced(ZERO_CALL_FUSED_STEP, s, [&] {
+                 return zero_fused_step(L, -1, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
+                                        a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, zs);
+             })) != ZERO_OK)
+            return rc;
+    } else {
+        // alternate only short buckets: a launch's ramp and drain cost a few
+        // microseconds, which matters at 5M elements per bucket and not at 500M
+        const bool two = nb > 1 && L->psi_pad / nb <= kAlternateMaxElems;
+        if (two && (rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+        for (int32_t b = nb - 1, i = 0; b >= 0; --b, ++i) {  // last bucket first
+            const cudaStream_t sb = (two && (i & 1)) ? R.aux : s;
+            const zero_stream_t zb = reinterpret_cast<zero_stream_t>(sb);
+            if ((rc = ready(b, sb)) != ZERO_OK) return rc;
+            if (a->fused)
+                rc = traced(ZERO_CALL_FUSED_STEP, sb, [&] {
+                    return zero_fused_step(L, b, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
+                                           a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, zb);
+                });
+            else
+                rc = traced(ZERO_CALL_REDUCE_SCATTER, sb, [&] {
+                    return zero_reduce_scatter(L, b, a->grad_replicas, a->grad_shards, a->state, a->workspace, zb);
+                });
+            if (rc != ZERO_OK) return rc;
+        }
+        if (two && (rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
+    }
+    if (a->fused)
+        return traced(ZERO_CALL_GRAD_NORM, s, [&] {
+            return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, zs);
+        });
+    if ((rc = traced(ZERO_CALL_GRAD_NORM, s, [&] {
+             return zero_grad_norm(L, a->max_norm, ZERO_NORM_DECIDE, a->state, a->workspace, zs);
+         })) != ZERO_OK)
+        return rc;
+    if (!a->param16_shards)
+        return traced(ZERO_CALL_ADAMW, s, [&] {
+            return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards,
+                                         a->state, a->param16_full, ZERO_OUT_FULL_REPLICAS, zs);
+        });
+    if ((rc = traced(ZERO_CALL_ADAMW, s, [&] {
+             return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards,
+                                          a->state, a->param16_shards, ZERO_OUT_SHARDS, zs);
+         })) != ZERO_OK)
+        return rc;
+    return traced(ZERO_CALL_ALLGATHER, s, [&] {
+        return zero_allgather_params(L, (const void* const*)a->param16_shards, a->param16_full, zs);
+    });
 }
 
 }  // namespace
@@ -149,14 +304,20 @@ extern "C" zero_status_t zero_step(const zero_layout* L, const zero_step_args* a
     clear_error();
     zero_status_t rc = check_args(L, a, "zero_step");
     if (rc != ZERO_OK) return rc;
-    return run_step(L, a, stream, [](int32_t) { return ZERO_OK; });
+    DeviceRes* R = nullptr;
+    if ((rc = current_res(&R, "zero_step")) != ZERO_OK) return rc;
+    std::lock_guard<std::mutex> lock(R->mu);  // the fork/join events are shared by the device's calls
+    if ((rc = step_res(*R, "zero_step")) != ZERO_OK) return rc;
+    return run_step(L, a, reinterpret_cast<cudaStream_t>(stream), *R,
+                    [](int32_t, cudaStream_t) { return ZERO_OK; });
 }
 
 extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* a,
                                              const void* const* host_grads, int64_t chunk_elems,
                                              void* host_state, zero_stream_t stream) {
     clear_error();
-    zero_status_t rc = check_args(L, a, "zero_step_from_host");
+    const char* what = "zero_step_from_host";
+    zero_status_t rc = check_args(L, a, what);
     if (rc != ZERO_OK) return rc;
     if (!host_grads) return fail(ZERO_ERR_INVALID, "zero_step_from_host: NULL host gradient array");
     if (!a->grad_replicas) return fail(ZERO_ERR_INVALID, "zero_step_from_host: NULL device gradient array");
@@ -165,20 +326,25 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
         if (!a->grad_replicas[r]) return fail(ZERO_ERR_INVALID, "zero_step_from_host: NULL device gradient replica");
     }
     if (chunk_elems <= 0) chunk_elems = (int64_t)1 << 27;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail("zero_step_from_host", e);
-    if (dev < 0 || dev >= 64) return fail(ZERO_ERR_CUDA, "zero_step_from_host: device index >= 64");
-    const int32_t nb = (int32_t)L->buckets.size();
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-    std::lock_guard<std::mutex> lock(g_copy_mu);  // the events are reused by every call on this device
-    CopyStreams* c = nullptr;
-    if ((rc = copy_streams(dev, 2 * (size_t)nb, &c)) != ZERO_OK) return rc;
-    // the previous step on `stream` has finished reading the replicas before they are overwritten
-    if ((e = cudaEventRecord(c->start, s)) != cudaSuccess) return cuda_fail("zero_step_from_host: record", e);
+    DeviceRes* R = nullptr;
+    if ((rc = current_res(&R, what)) != ZERO_OK) return rc;
+    std::lock_guard<std::mutex> lock(R->mu);  // the events are reused by every call on this device
+    if ((rc = step_res(*R, what)) != ZERO_OK) return rc;
     for (int i = 0; i < 2; ++i)
-        if ((e = cudaStreamWaitEvent(c->cs[i], c->start, 0)) != cudaSuccess)
+        if ((rc = make_stream(&R->cs[i], what)) != ZERO_OK) return rc;
+    if ((rc = make_event(&R->start, what)) != ZERO_OK) return rc;
+    const int32_t nb = (int32_t)L->buckets.size();
+    while (R->ev.size() < 2 * (size_t)nb) {
+        cudaEvent_t x = nullptr;
+        if ((rc = make_event(&x, what)) != ZERO_OK) return rc;
+        R->ev.push_back(x);
+    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    // the previous step on `stream` has finished reading the replicas before they are overwritten
+    if ((e = cudaEventRecord(R->start, s)) != cudaSuccess) return cuda_fail("zero_step_from_host: record", e);
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(R->cs[i], R->start, 0)) != cudaSuccess)
             return cuda_fail("zero_step_from_host: wait", e);
     // copies in the order the step consumes the buckets (units): last first
     const size_t esz = sizeof(uint16_t);
@@ -190,17 +356,17 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
                 const int64_t n = (hi - off) < chunk_elems ? (hi - off) : chunk_elems;
                 e = cudaMemcpyAsync(static_cast<char*>(const_cast<void*>(a->grad_replicas[r])) + off * esz,
                                     static_cast<const char*>(host_grads[r]) + off * esz, (size_t)n * esz,
-                                    cudaMemcpyHostToDevice, c->cs[i % 2]);
+                                    cudaMemcpyHostToDevice, R->cs[i % 2]);
                 if (e != cudaSuccess) return cuda_fail("zero_step_from_host: host-to-device copy", e);
             }
         }
         for (int q = 0; q < 2; ++q)
-            if ((e = cudaEventRecord(c->ev[2 * k + q], c->cs[q])) != cudaSuccess)
+            if ((e = cudaEventRecord(R->ev[2 * k + q], R->cs[q])) != cudaSuccess)
                 return cuda_fail("zero_step_from_host: record", e);
     }
-    rc = run_step(L, a, stream, [&](int32_t k) -> zero_status_t {
+    rc = run_step(L, a, s, *R, [&](int32_t k, cudaStream_t on) -> zero_status_t {
         for (int q = 0; q < 2; ++q) {
-            cudaError_t w = cudaStreamWaitEvent(s, c->ev[2 * k + q], 0);
+            cudaError_t w = cudaStreamWaitEvent(on, R->ev[2 * k + q], 0);
             if (w != cudaSuccess) return cuda_fail("zero_step_from_host: wait", w);
         }
         return ZERO_OK;
@@ -209,6 +375,56 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
     if (host_state) {
         e = cudaMemcpyAsync(host_state, a->state, sizeof(zero_step_state), cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail("zero_step_from_host: state read-back", e);
+    }
+    return ZERO_OK;
+}
+
+extern "C" int32_t zero_trace_enable(int32_t on) { return g_trace_on.exchange(on ? 1 : 0); }
+
+extern "C" zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset) {
+    clear_error();
+    if (!out) return fail(ZERO_ERR_INVALID, "zero_trace_read: NULL output");
+    *out = zero_trace_totals{};
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    // busy time per kind: the union of its calls' intervals, placed on one
+    // time axis per device by their offsets from that device's first event
+    std::vector<std::pair<double, double>> spans[ZERO_CALL_KINDS];
+    cudaEvent_t ref[64] = {nullptr};
+    for (const TraceRecord& t : g_trace) {
+        cudaError_t e = cudaEventSynchronize(t.e1);
+        float ms = 0.0f, at = 0.0f;
+        if (!ref[t.dev]) ref[t.dev] = t.e0;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.e0, t.e1);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&at, ref[t.dev], t.e0);
+        if (e != cudaSuccess) return cuda_fail("zero_trace_read", e);
+        if (t.kind >= 0 && t.kind < ZERO_CALL_KINDS) {
+            out->calls[t.kind] += 1;
+            out->total_ms[t.kind] += ms;
+            spans[t.kind].push_back({(double)at + 1e6 * t.dev, (double)at + 1e6 * t.dev + ms});
+        }
+    }
+    for (int k = 0; k < ZERO_CALL_KINDS; ++k) {
+        auto& v = spans[k];
+        std::sort(v.begin(), v.end());
+        double busy = 0.0, lo = 0.0, hi = -1.0;
+        for (const auto& p : v) {
+            if (p.first > hi) {
+                if (hi > lo) busy += hi - lo;
+                lo = p.first;
+                hi = p.second;
+            } else if (p.second > hi) {
+                hi = p.second;
+            }
+        }
+        if (hi > lo) busy += hi - lo;
+        out->busy_ms[k] = busy;
+    }
+    if (reset) {
+        for (const TraceRecord& t : g_trace) {
+            g_trace_free[t.dev].push_back(t.e0);
+            g_trace_free[t.dev].push_back(t.e1);
+        }
+        g_trace.clear();
     }
     return ZERO_OK;
 }
