@@ -362,6 +362,12 @@ typedef struct zero_step_args {
     void* const* transient;             /* ZeRO-3: transient unit buffers (largest unit) */
     zero_step_state* state;             /* device */
     void* workspace;                    /* device, zero_layout_info.workspace_bytes */
+    void* const* transient2;            /* ZeRO-3, optional: a second set of transient
+                                           buffers.  Consecutive units then alternate
+                                           buffers and streams (two live units, [L5]
+                                           §4 prefetch): a unit's gather overlaps the
+                                           previous unit's reduce-scatter and update.
+                                           NULL: one buffer, one stream */
 } zero_step_args;
 
 /* One whole step with the gradient replicas resident in device memory, in the
@@ -375,7 +381,9 @@ typedef struct zero_step_args {
  *   ZeRO-3: zero_stage3_gather_layer for units 0..U-1 (forward), then for
  *     u = U-1..0: gather u again and zero_fused_step(u) (fused) or
  *     zero_reduce_scatter(u) (split, followed by the norm and the shard
- *     update after the loop).
+ *     update after the loop).  With transient2, units alternate between the
+ *     two buffer sets and between `stream` and the library's second stream;
+ *     every forward gather ends before the first update.
  * ZeRO-1/2 bucket launches alternate between `stream` and a second stream of
  * the library's (one per device, created at the first call), which joins
  * `stream` again before the norm: consecutive buckets touch disjoint elements

@@ -41,10 +41,10 @@ def test_host_input_garbage_padding():
     run_parity(c, 2, garbage_pads=True, host_input=True)
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_host_input_zero3(fused):
+@pytest.mark.parametrize("fused,live", [(True, 1), (False, 1), (True, 2), (False, 2)])
+def test_host_input_zero3(fused, live):
     c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS, max_norm=0.0 if fused else 0.05)
-    run_parity(c, 2, host_input=10_000, use_gpu_clip=not fused)
+    run_parity(c, 2, host_input=10_000, use_gpu_clip=not fused, live_units=live)
 
 
 def test_host_input_equals_device_step():

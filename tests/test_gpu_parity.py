@@ -487,3 +487,16 @@ def test_launch_tracing_counts_every_call_of_the_executor():
         Bd.zero_trace_enable(False)
     t = Bd.zero_trace_read(reset=True)
     assert t["fused_step"]["launches"] == f.n_buckets and t["grad_norm"]["launches"] == 1
+
+
+@pytest.mark.parametrize("fused,fmt", [(True, FMT_BF16), (False, FMT_FP16)])
+def test_zero3_two_live_units_equal_one(fused, fmt):
+    # zero_step with a second transient set (units alternate buffers and streams) against one buffer
+    # and against the oracle, bit for bit
+    kw = {} if fused else dict(max_norm=0.01, loss_scale=512.0, dynamic=True)
+    c = Case(Z3_NUMELS, 4, 3, fmt, units=Z3_UNITS, per_tensor_scale=True, **kw)
+    e2, zs, _ = run_parity(c, 3, live_units=2)
+    assert e2.transient2 is not None
+    e1, _, _ = run_parity(c, 3)
+    for name in ("master", "m", "v", "shard16", "state"):
+        assert torch.equal(getattr(e1, name), getattr(e2, name)), name

@@ -95,7 +95,8 @@ class zero_step_args(ctypes.Structure):
                [(n, ctypes.POINTER(ctypes.c_void_p)) for n in
                 ("grad_replicas", "master", "m", "v", "grad_shards", "param16_full", "param16_shards",
                  "transient")] + \
-               [("state", ctypes.c_void_p), ("workspace", ctypes.c_void_p)]
+               [("state", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("transient2", ctypes.POINTER(ctypes.c_void_p))]
 
 
 class StepArgs:
@@ -104,13 +105,14 @@ class StepArgs:
 
     def __init__(self, L: "Layout", hp: zero_adamw_hp, max_norm: float, fused: bool, per_bucket: bool,
                  grad_replicas, master, m, v, grad_shards, param16_full, param16_shards, transient, st,
-                 workspace):
+                 workspace, transient2=None):
         self._keep = [hp]
         self.args = zero_step_args(hp=ctypes.pointer(hp), max_norm=float(max_norm), fused=int(bool(fused)),
                                    per_bucket=int(bool(per_bucket)), state=_addr(st), workspace=_addr(workspace))
         for name, xs in (("grad_replicas", grad_replicas), ("master", master), ("m", m), ("v", v),
                          ("grad_shards", grad_shards), ("param16_full", param16_full),
-                         ("param16_shards", param16_shards), ("transient", transient)):
+                         ("param16_shards", param16_shards), ("transient", transient),
+                         ("transient2", transient2)):
             arr = _ptrs(xs, L)
             if arr is not None:
                 self._keep.append(arr)

@@ -80,6 +80,8 @@ zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const ch
     if ((rc = check_ptrs((const void* const*)a->param16_full, n, w + " param16_full")) != ZERO_OK) return rc;
     if ((rc = check_ptrs((const void* const*)a->param16_shards, n, w + " param16_shards")) != ZERO_OK) return rc;
     if ((rc = check_ptrs((const void* const*)a->transient, n, w + " transient")) != ZERO_OK) return rc;
+    if (a->transient2 && L->stage != 3) return fail(ZERO_ERR_INVALID, w + ": transient2 is for ZeRO-3 only");
+    if ((rc = check_ptrs((const void* const*)a->transient2, n, w + " transient2")) != ZERO_OK) return rc;
     const void* one[2] = {a->state, a->workspace};
     if (!a->state || !a->workspace) return fail(ZERO_ERR_INVALID, w + ": NULL state or workspace");
     return check_ptrs(one, 2, w + " state/workspace");
@@ -201,36 +203,64 @@ constexpr int64_t kAlternateMaxElems = (int64_t)1 << 25;
 // the SMs that the previous bucket's last CTAs free, instead of after its
 // whole grid has drained.  The second stream joins `s` before the global
 // norm.  Results do not depend on it (every output element and partial has
-// one writer).  ZeRO-3 units share one transient buffer and stay on `s`.
+// one writer).
 zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
                        const Ready& ready) {
     zero_status_t rc;
     const int32_t nb = (int32_t)L->buckets.size();
     const zero_stream_t zs = reinterpret_cast<zero_stream_t>(s);
     if (L->stage == 3) {
+        // One transient buffer: every unit on `s`.  Two (transient2): the
+        // pages' prefetch with two live units -- consecutive units alternate
+        // buffers and streams, so a unit's gather runs while the previous
+        // unit's reduce-scatter and update drain.  A unit's gather and its
+        // update stay on one stream (the update rewrites the 16-bit shard the
+        // gather reads); units sharing a buffer share a stream; the second
+        // stream joins `s` after the forward gathers and again before the norm.
         const int32_t U = (int32_t)L->segs.size();
-        for (int32_t u = 0; u < U; ++u)  // forward
-            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, s, [&] {
-                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, zs);
+        const bool two = a->transient2 != nullptr && U > 1;
+        auto lane = [&](int32_t i, cudaStream_t& st, void* const*& buf) {
+            const bool odd = two && (i & 1);
+            st = odd ? R.aux : s;
+            buf = odd ? a->transient2 : a->transient;
+        };
+        if (two && (rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+        for (int32_t u = 0; u < U; ++u) {  // forward
+            cudaStream_t st;
+            void* const* buf;
+            lane(u, st, buf);
+            const zero_stream_t zst = reinterpret_cast<zero_stream_t>(st);
+            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, st, [&] {
+                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, buf, zst);
                  })) != ZERO_OK)
                 return rc;
-        for (int32_t u = U - 1; u >= 0; --u) {  // backward
-            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, s, [&] {
-                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, a->transient, zs);
+        }
+        if (two) {  // forward reads of every unit end before any update rewrites a shard
+            if ((rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
+            if ((rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+        }
+        for (int32_t u = U - 1, i = 0; u >= 0; --u, ++i) {  // backward
+            cudaStream_t st;
+            void* const* buf;
+            lane(i, st, buf);
+            const zero_stream_t zst = reinterpret_cast<zero_stream_t>(st);
+            if ((rc = traced(ZERO_CALL_STAGE3_GATHER, st, [&] {
+                     return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, buf, zst);
                  })) != ZERO_OK)
                 return rc;
-            if ((rc = ready(u, s)) != ZERO_OK) return rc;
+            if ((rc = ready(u, st)) != ZERO_OK) return rc;
             if (a->fused)
-                rc = traced(ZERO_CALL_FUSED_STEP, s, [&] {
+                rc = traced(ZERO_CALL_FUSED_STEP, st, [&] {
                     return zero_fused_step(L, u, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                           a->param16_shards, ZERO_OUT_SHARDS, a->workspace, zs);
+                                           a->param16_shards, ZERO_OUT_SHARDS, a->workspace, zst);
                 });
             else
-                rc = traced(ZERO_CALL_REDUCE_SCATTER, s, [&] {
-                    return zero_reduce_scatter(L, u, a->grad_replicas, a->grad_shards, a->state, a->workspace, zs);
+                rc = traced(ZERO_CALL_REDUCE_SCATTER, st, [&] {
+                    return zero_reduce_scatter(L, u, a->grad_replicas, a->grad_shards, a->state, a->workspace, zst);
                 });
             if (rc != ZERO_OK) return rc;
         }
+        if (two && (rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
         if (a->fused)
             return traced(ZERO_CALL_GRAD_NORM, s, [&] {
                 return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, zs);

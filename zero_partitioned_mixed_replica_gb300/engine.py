@@ -53,7 +53,7 @@ class ZeroStep:
                  dynamic_scale: bool = False, growth_interval: int = 2000,
                  fused: Optional[bool] = None, per_bucket: bool = True, fuse_allgather: bool = True,
                  n_micro: int = 1, device: str = "cuda", stream: Optional[torch.cuda.Stream] = None,
-                 pad_multiple: int = 0):
+                 pad_multiple: int = 0, live_units: int = 1):
         if stage not in (1, 2, 3):
             raise ValueError("ZeroStep runs ZeRO stages 1, 2 and 3")
         self.pad_multiple = pad_multiple    # 0: N_d * 128; else a multiple of it
@@ -102,10 +102,14 @@ class ZeroStep:
             self.shard16 = torch.zeros(n_d, S, dtype=dt16, device=dev)
             max_real = max(u.real for u in self.units)
             self.transient = torch.zeros(n_d, (max_real + 127) // 128 * 128, dtype=dt16, device=dev)
+            # live_units = 2: a second transient per rank, so that zero_step gathers the next unit
+            # while the previous one is reduced and updated ("第 5 课" §4 prefetch, two live units)
+            self.transient2 = torch.zeros_like(self.transient) if live_units >= 2 else None
         else:
             self.params = torch.zeros(n_d, P, dtype=dt16, device=dev)
             self.shard16 = None if self.fuse_allgather else torch.zeros(n_d, S, dtype=dt16, device=dev)
             self.transient = None
+            self.transient2 = None
         self.workspace = torch.zeros(self.info.workspace_bytes, dtype=torch.uint8, device=dev)
         self.state = torch.zeros(96, dtype=torch.uint8, device=dev)
         self._rows()
@@ -135,6 +139,7 @@ class ZeroStep:
         self.param_rows = rows(self.params)
         self.shard16_rows = rows(self.shard16)
         self.transient_rows = rows(self.transient)
+        self.transient2_rows = rows(self.transient2)
         self.acc_rows = rows(getattr(self, "acc", None))
 
     def _s(self):
@@ -191,7 +196,8 @@ class ZeroStep:
                 self.grad_rows, self.master_rows, self.m_rows, self.v_rows,
                 None if self.fused else self.gshard_rows, None if stage3 else self.param_rows,
                 self.shard16_rows if (stage3 or not self.fuse_allgather) else None,
-                self.transient_rows if stage3 else None, self.state, self.workspace)
+                self.transient_rows if stage3 else None, self.state, self.workspace,
+                self.transient2_rows if stage3 else None)
         return self._args
 
     def step(self) -> None:
