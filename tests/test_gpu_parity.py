@@ -5,7 +5,8 @@ Sizes span many CTAs and grid-stride rounds with ragged tails (padding inside
 the last vector, buckets that straddle shards, units of different sizes).
 The bar: step flags, counters and loss scale bit-exact; fp32 master/m/v within
 1e-6 relative (|x| < 1e-30 absolutely within 1e-36); 16-bit parameters within
-1 ulp; the global norm within 1e-5 relative.  Bitwise equality of the state is
+1 ulp; the global norm within 1e-5 relative (and within 2^-25, the rounding of
+the binary32 partials).  Bitwise equality of the state is
 also asserted wherever GPU and oracle used the same clip coefficient (always,
 when the oracle is re-run with the GPU's coefficient)."""
 import math
@@ -100,7 +101,10 @@ def run_parity(case: Case, steps: int, garbage_pads: bool = False, use_gpu_clip:
             assert math.isinf(g["grad_norm"])
         else:
             assert g["grad_norm"] == pytest.approx(o["norm"], rel=1e-5, abs=1e-30)
-            assert abs(g["grad_norm"] - o["norm"]) <= 1e-9 * o["norm"] + 1e-30  # aim: far inside the bar
+            # far inside the bar: each 32-element partial is one binary32 (relative error <= 2^-24
+            # on the sum of squares, 2^-25 on the norm); with many partials the errors average out
+            # (<= 1e-9 measured), with one partial (Psi = 1) the whole 2^-25 can show
+            assert abs(g["grad_norm"] - o["norm"]) <= 2.0 ** -25 * (1 + 1e-6) * o["norm"] + 1e-30
         same_clip = np.float32(g["clip_coef"]) == np.float32(o["clip"])
         for name in ("master", "m", "v"):
             gpu = eng.flat(name).cpu().numpy()
@@ -500,3 +504,17 @@ def test_zero3_two_live_units_equal_one(fused, fmt):
     e1, _, _ = run_parity(c, 3)
     for name in ("master", "m", "v", "shard16", "state"):
         assert torch.equal(getattr(e1, name), getattr(e2, name)), name
+
+
+@pytest.mark.parametrize("n_d,stage,fmt,max_norm", [(1, 2, FMT_BF16, 0.0), (1, 1, FMT_FP16, 1e-4), (3, 2, FMT_BF16, 0.0),
+                                                    (64, 2, FMT_FP16, 1e-4), (64, 3, FMT_BF16, 0.0),
+                                                    (2, 3, FMT_FP16, 1e-4)])
+def test_single_parameter_buffers(n_d, stage, fmt, max_norm):
+    # Psi = 1: one real element and q - 1 padding elements; every rank but rank 0 owns only padding
+    units = [0] if stage == 3 else None
+    c = Case([1], n_d, stage, fmt, units=units, max_norm=max_norm, loss_scale=2.0 ** 10 if fmt == FMT_FP16 else 1.0,
+             dynamic=fmt == FMT_FP16)
+    eng, zs, hist = run_parity(c, 3, garbage_pads=True)
+    assert eng.info.psi == 1 and eng.info.psi_pad == n_d * 128
+    if max_norm > 0:
+        assert all(g["clip_coef"] == o["clip"] for g, o in hist)
