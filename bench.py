@@ -393,9 +393,15 @@ def gpu_run(args, w, rank, world, local_rank):
                 eng.micro_step(mb)
     else:
         run = (lambda: graph.replay()) if graph is not None else eng.step
+    # the warm-up steps run traced too, so that the timed steps reuse the trace's events
+    # instead of creating them inside the timed region
+    trace = graph is None and args.micro == 1
+    B.zero_trace_enable(trace)
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize(dev)
+    B.zero_trace_enable(False)
+    B.zero_trace_read(reset=True)
     # --- timed region -----------------------------------------------------------
     if world > 1:
         dist.barrier()
@@ -409,11 +415,9 @@ def gpu_run(args, w, rank, world, local_rank):
     # per-call durations from CUDA events on each call's launching stream: the library's
     # launch tracing for the step executor (zero_step); the engine's own per-call events
     # for the micro-batch calls it issues itself
-    trace = graph is None and args.micro == 1
     if graph is None and args.micro > 1:
         eng.timers = {}
     if trace:
-        B.zero_trace_read(reset=True)
         B.zero_trace_enable(True)
     B.zero_launch_count(reset=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -384,9 +384,10 @@ typedef struct zero_step_args {
  *     update after the loop).  With transient2, units alternate between the
  *     two buffer sets and between `stream` and the library's second stream;
  *     every forward gather ends before the first update.
- * ZeRO-1/2 bucket launches alternate between `stream` and a second stream of
- * the library's (one per device, created at the first call), which joins
- * `stream` again before the norm: consecutive buckets touch disjoint elements
+ * ZeRO-1/2 bucket launches of short buckets (mean at most 2^27 elements)
+ * alternate between `stream` and a second stream of the library's (one per
+ * device, created at the first call), which joins `stream` again before the
+ * norm: consecutive buckets touch disjoint elements
  * and norm-partial slots, so one bucket's launch can start while the previous
  * one drains.  Results do not depend on it.
  * Asynchronous on `stream`; allocates no device memory; captures into a CUDA
@@ -422,7 +423,8 @@ zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* ar
  * every library call the executor issues is bracketed by two timing events
  * recorded on the stream the call is issued on (none while that stream is
  * being captured into a CUDA graph); zero_trace_read waits for the recorded
- * events and adds up the elapsed time per kind of call. */
+ * events and adds up the elapsed time per kind of call.  Records accumulate
+ * until a read with reset; beyond 2^20 of them, calls run untraced. */
 enum {
     ZERO_CALL_REDUCE_SCATTER = 0,
     ZERO_CALL_GRAD_NORM = 1,      /* both passes of zero_grad_norm */

@@ -516,5 +516,6 @@ def test_single_parameter_buffers(n_d, stage, fmt, max_norm):
              dynamic=fmt == FMT_FP16)
     eng, zs, hist = run_parity(c, 3, garbage_pads=True)
     assert eng.info.psi == 1 and eng.info.psi_pad == n_d * 128
-    if max_norm > 0:
-        assert all(g["clip_coef"] == o["clip"] for g, o in hist)
+    if max_norm > 0:    # the coefficients agree to one binary32 rounding (the norm's partial, above)
+        assert all(0 < g["clip_coef"] <= 1 and abs(g["clip_coef"] - o["clip"]) <= 2.0 ** -23 * o["clip"]
+                   for g, o in hist if not g["overflow"])

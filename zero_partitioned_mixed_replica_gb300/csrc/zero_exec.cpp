@@ -92,6 +92,9 @@ zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const ch
 // bracketed by two timing events recorded on the stream it is issued on
 // (not while that stream is being captured into a graph).
 // ---------------------------------------------------------------------------
+// At most this many calls are kept between reads; later calls run untraced.
+constexpr size_t kTraceMaxRecords = (size_t)1 << 20;
+
 struct TraceRecord {
     int32_t kind;
     int32_t dev;
@@ -123,7 +126,7 @@ zero_status_t traced(int32_t kind, cudaStream_t st, Call&& call) {
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_trace_mu);
-        if (!trace_take(dev, &e0)) return call();
+        if (g_trace.size() >= kTraceMaxRecords || !trace_take(dev, &e0)) return call();
         if (!trace_take(dev, &e1)) {
             g_trace_free[dev].push_back(e0);
             return call();
@@ -187,11 +190,41 @@ zero_status_t wait_on(cudaStream_t waiter, cudaEvent_t ev, cudaStream_t recorder
     return e == cudaSuccess ? ZERO_OK : cuda_fail(what, e);
 }
 
+// The device's second stream, forked from `s` (it waits for the work queued
+// on `s`) and joined back (`s` waits for it) explicitly or, if a call of the
+// step fails in between, when the fork goes out of scope: the caller's
+// stream never runs ahead of work left on the second stream.
+class Fork {
+  public:
+    Fork(cudaStream_t s, DeviceRes& R) : s_(s), R_(R) {}
+    zero_status_t open() {
+        zero_status_t rc = wait_on(R_.aux, R_.fork, s_, "zero_step: fork");
+        open_ = rc == ZERO_OK;
+        return rc;
+    }
+    zero_status_t join() {
+        if (!open_) return ZERO_OK;
+        open_ = false;
+        return wait_on(s_, R_.join, R_.aux, "zero_step: join");
+    }
+    ~Fork() {  // after a failed call: join without replacing that call's error message
+        if (open_ && cudaEventRecord(R_.join, R_.aux) == cudaSuccess) cudaStreamWaitEvent(s_, R_.join, 0);
+    }
+
+  private:
+    cudaStream_t s_;
+    DeviceRes& R_;
+    bool open_ = false;
+};
+
 using Ready = std::function<zero_status_t(int32_t, cudaStream_t)>;
 
 // Mean bucket length up to which consecutive bucket launches alternate
-// between two streams.
-constexpr int64_t kAlternateMaxElems = (int64_t)1 << 25;
+// between two streams.  GB300, 350M layout, fused step: alternating raised
+// every bucket size measured, 1e5 to 5e7 elements (5e7 at N_d = 2: 6.11 TB/s
+// on one stream, 8 buckets); the 1.5B run's 500M-element buckets drain in
+// about 0.1% of a launch and stay on one stream.
+constexpr int64_t kAlternateMaxElems = (int64_t)1 << 27;
 
 // The step's calls on `s`.  ready(k, stream) runs before the first call that
 // reads the gradient replicas of bucket k (ZeRO-3: unit k), on the stream
@@ -224,7 +257,8 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             st = odd ? R.aux : s;
             buf = odd ? a->transient2 : a->transient;
         };
-        if (two && (rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+        Fork fork(s, R);
+        if (two && (rc = fork.open()) != ZERO_OK) return rc;
         for (int32_t u = 0; u < U; ++u) {  // forward
             cudaStream_t st;
             void* const* buf;
@@ -236,8 +270,8 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                 return rc;
         }
         if (two) {  // forward reads of every unit end before any update rewrites a shard
-            if ((rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
-            if ((rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+            if ((rc = fork.join()) != ZERO_OK) return rc;
+            if ((rc = fork.open()) != ZERO_OK) return rc;
         }
         for (int32_t u = U - 1, i = 0; u >= 0; --u, ++i) {  // backward
             cudaStream_t st;
@@ -260,7 +294,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                 });
             if (rc != ZERO_OK) return rc;
         }
-        if (two && (rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
+        if ((rc = fork.join()) != ZERO_OK) return rc;
         if (a->fused)
             return traced(ZERO_CALL_GRAD_NORM, s, [&] {
                 return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, zs);
@@ -285,9 +319,10 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             return rc;
     } else {
         // alternate only short buckets: a launch's ramp and drain cost a few
-        // microseconds, which matters at 5M elements per bucket and not at 500M
+        // microseconds, which matters at 5M-50M elements per bucket, not at 500M
         const bool two = nb > 1 && L->psi_pad / nb <= kAlternateMaxElems;
-        if (two && (rc = wait_on(R.aux, R.fork, s, "zero_step: fork")) != ZERO_OK) return rc;
+        Fork fork(s, R);
+        if (two && (rc = fork.open()) != ZERO_OK) return rc;
         for (int32_t b = nb - 1, i = 0; b >= 0; --b, ++i) {  // last bucket first
             const cudaStream_t sb = (two && (i & 1)) ? R.aux : s;
             const zero_stream_t zb = reinterpret_cast<zero_stream_t>(sb);
@@ -303,7 +338,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                 });
             if (rc != ZERO_OK) return rc;
         }
-        if (two && (rc = wait_on(s, R.join, R.aux, "zero_step: join")) != ZERO_OK) return rc;
+        if ((rc = fork.join()) != ZERO_OK) return rc;
     }
     if (a->fused)
         return traced(ZERO_CALL_GRAD_NORM, s, [&] {

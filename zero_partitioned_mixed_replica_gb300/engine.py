@@ -3,7 +3,9 @@
 :class:`ZeroStep` allocates every buffer once (torch is the allocator, in the
 spirit of the pre-allocated contiguous blocks of "ZeRO: Memory Optimizations
 Toward Training Trillion Parameter Models" reading notes §3.2.3/§5.3) and
-issues the library calls of one step in the order the pages give:
+runs a step as one call of the library's step executor (``zero_step``, or
+``zero_step_from_host`` for gradients in host memory), which issues the
+library calls in the order the pages give:
 
 * ZeRO-1/2, split (clipping or a loss scaler active): reduce-scatter bucket by
   bucket, last bucket first (backward produces the last layers first; mlqm.cn
@@ -18,8 +20,10 @@ issues the library calls of one step in the order the pages give:
   reading notes §3.1 and §4.3, "ZeRO-3 核心流程" §2).  With clipping or a scaler
   the shard updates wait for the global decision.
 
-Every arithmetic step runs inside libzero's kernels; this module only owns
-memory, orders the calls and reads back the 96-byte step state.
+The same calls can also be issued one by one from here (``_step``), for a
+per-call hook on the ZeRO-3 transients or per-call timers; results are
+identical.  Every arithmetic step runs inside libzero's kernels; this module
+only owns memory, orders calls and reads back the 96-byte step state.
 """
 from __future__ import annotations
 
@@ -188,8 +192,10 @@ class ZeroStep:
     # -- the step ------------------------------------------------------------------
     def step_args(self) -> B.StepArgs:
         """This engine's buffers and settings as the library's zero_step_args
-        (built once: the buffers never move)."""
-        if getattr(self, "_args", None) is None:
+        (built once, as the buffers never move; built again if ``hp`` is
+        replaced by another object)."""
+        if getattr(self, "_args", None) is None or self._args_hp is not self.hp:
+            self._args_hp = self.hp
             stage3 = self.stage == 3
             self._args = B.StepArgs(
                 self.L, self.hp, self.max_norm if not self.fused else 0.0, self.fused, self.per_bucket,
