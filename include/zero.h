@@ -338,6 +338,16 @@ zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
 /* ------------------------------------------------------------------------ */
 /* The whole step in one call                                                */
 /* ------------------------------------------------------------------------ */
+/* Called by the step executor on the calling thread right after it has
+ * issued the gather of ZeRO-3 unit `unit` on `stream` (pass 0: forward, 1:
+ * backward), before it issues anything else for that unit: the place where a
+ * layer's forward or backward computation on the gathered unit would be
+ * enqueued.  `transient` holds the N_d buffers that gather writes.  The hook
+ * must not call zero_step or zero_step_from_host (the executor holds its
+ * per-device lock). */
+typedef void (*zero_unit_hook_fn)(void* user, int32_t pass, int32_t unit, void* const* transient,
+                                  zero_stream_t stream);
+
 /* Buffers and settings of one step, for zero_step and zero_step_from_host.
  * Every pointer array holds N_d device pointers (256-byte aligned); the
  * library reads the arrays during the call only. */
@@ -368,6 +378,8 @@ typedef struct zero_step_args {
                                            §4 prefetch): a unit's gather overlaps the
                                            previous unit's reduce-scatter and update.
                                            NULL: one buffer, one stream */
+    zero_unit_hook_fn unit_hook;        /* ZeRO-3, optional: see zero_unit_hook_fn */
+    void* hook_user;                    /* passed to unit_hook */
 } zero_step_args;
 
 /* One whole step with the gradient replicas resident in device memory, in the

@@ -213,3 +213,27 @@ def test_executor_and_cast_validate_before_launch():
     assert status(B.zero_cast_params, L, two, two, 5, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_cast_params, L, [FAKE, MIS], two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_ALIGN
     assert status(B.zero_cast_params, L0, two, two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_STATE
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    # every struct the binding mirrors has the header's size and field offsets (plain C compiler)
+    import subprocess
+    structs = {"zero_step_args": B.zero_step_args, "zero_step_state": B.zero_step_state,
+               "zero_trace_totals": B.zero_trace_totals, "zero_layout_info": B.zero_layout_info,
+               "zero_unit_info": B.zero_unit_info, "zero_adamw_hp": B.zero_adamw_hp,
+               "zero_copy_segment": B.zero_copy_segment}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "zero.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (name, name))
+        for f in cls._fields_:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (name, f[0], name, f[0]))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == ctypes.sizeof(cls), name
+        for f in cls._fields_:
+            assert int(got["%s.%s" % (name, f[0])]) == getattr(cls, f[0]).offset, (name, f[0])

@@ -421,11 +421,55 @@ def test_cast_params_matches_oracle_cast(n_d, stage, fmt):
         assert not _u16(eng.params[0])[pad].any()
 
 
+def _issue_step_calls(eng, s=None):
+    """The step's calls issued one by one through the C ABI, in the pages' order
+    as the test restates it: ZeRO-1/2 reduce-scatter (or fused step) per bucket,
+    last bucket first, then the norm and, split, AdamW (fused or unfused
+    all-gather); ZeRO-3 forward gathers, then per unit in reverse a gather and a
+    fused step or reduce-scatter, then the norm (and, split, the shard update)."""
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    L = eng.L
+    s = s or torch.cuda.current_stream()
+    if eng.stage == 3:
+        U = len(eng.units)
+        for u in list(range(U)) + list(reversed(range(U))):
+            Bd.zero_stage3_gather_layer(L, u, eng.shard16_rows, eng.transient_rows, s)
+        for u in reversed(range(U)):
+            if eng.fused:
+                Bd.zero_fused_step(L, u, eng.hp, eng.grad_rows, eng.master_rows, eng.m_rows, eng.v_rows, eng.state,
+                                   eng.shard16_rows, Bd.ZERO_OUT_SHARDS, eng.workspace, s)
+            else:
+                Bd.zero_reduce_scatter(L, u, eng.grad_rows, eng.gshard_rows, eng.state, eng.workspace, s)
+        if eng.fused:
+            Bd.zero_grad_norm(L, 0.0, Bd.ZERO_NORM_AFTER_FUSED, eng.state, eng.workspace, s)
+        else:
+            Bd.zero_grad_norm(L, eng.max_norm, Bd.ZERO_NORM_DECIDE, eng.state, eng.workspace, s)
+            Bd.zero_adamw_shard_step(L, eng.hp, eng.master_rows, eng.m_rows, eng.v_rows, eng.gshard_rows,
+                                     eng.state, eng.shard16_rows, Bd.ZERO_OUT_SHARDS, s)
+        return
+    if eng.fused:
+        for b in (reversed(range(eng.n_buckets)) if eng.per_bucket else [-1]):
+            Bd.zero_fused_step(L, b, eng.hp, eng.grad_rows, eng.master_rows, eng.m_rows, eng.v_rows, eng.state,
+                               eng.param_rows, Bd.ZERO_OUT_FULL_REPLICAS, eng.workspace, s)
+        Bd.zero_grad_norm(L, 0.0, Bd.ZERO_NORM_AFTER_FUSED, eng.state, eng.workspace, s)
+        return
+    for b in reversed(range(eng.n_buckets)):
+        Bd.zero_reduce_scatter(L, b, eng.grad_rows, eng.gshard_rows, eng.state, eng.workspace, s)
+    Bd.zero_grad_norm(L, eng.max_norm, Bd.ZERO_NORM_DECIDE, eng.state, eng.workspace, s)
+    if eng.fuse_allgather:
+        Bd.zero_adamw_shard_step(L, eng.hp, eng.master_rows, eng.m_rows, eng.v_rows, eng.gshard_rows, eng.state,
+                                 eng.param_rows, Bd.ZERO_OUT_FULL_REPLICAS, s)
+    else:
+        Bd.zero_adamw_shard_step(L, eng.hp, eng.master_rows, eng.m_rows, eng.v_rows, eng.gshard_rows, eng.state,
+                                 eng.shard16_rows, Bd.ZERO_OUT_SHARDS, s)
+        Bd.zero_allgather_params(L, eng.shard16_rows, eng.param_rows, s)
+
+
 @pytest.mark.parametrize("mode", ["z2_fused_bucket", "z2_fused_whole", "z2_split_clip_fp16", "z1_split_unfused_ag",
-                                  "z3_fused", "z3_split_fp16"])
+                                  "z3_fused", "z3_split_fp16", "z3_fused_two_live"])
 def test_native_executor_equals_call_by_call(mode):
-    # zero_step (the library issues the step's calls) against the same calls issued one by one
-    # from Python (the path the per-kernel timers use): bit-identical state after 3 steps
+    # zero_step (the library issues the step's calls: alternating bucket streams, two live units)
+    # against the same calls issued one by one on one stream: bit-identical state after 3 steps
     kw = {"z2_fused_bucket": dict(n_d=4, stage=2, fmt=FMT_BF16, eng=dict(per_bucket=True)),
           "z2_fused_whole": dict(n_d=4, stage=2, fmt=FMT_BF16, eng=dict(per_bucket=False)),
           "z2_split_clip_fp16": dict(n_d=8, stage=2, fmt=FMT_FP16, max_norm=0.05, loss_scale=4096.0, dynamic=True,
@@ -433,7 +477,8 @@ def test_native_executor_equals_call_by_call(mode):
           "z1_split_unfused_ag": dict(n_d=3, stage=1, fmt=FMT_BF16, max_norm=0.05, eng=dict(fuse_allgather=False)),
           "z3_fused": dict(n_d=2, stage=3, fmt=FMT_BF16, eng={}),
           "z3_split_fp16": dict(n_d=4, stage=3, fmt=FMT_FP16, max_norm=0.01, loss_scale=256.0, dynamic=True,
-                                eng={})}[mode]
+                                eng={}),
+          "z3_fused_two_live": dict(n_d=2, stage=3, fmt=FMT_BF16, eng=dict(live_units=2))}[mode]
     ekw = kw.pop("eng")
     n_d, stage, fmt = kw.pop("n_d"), kw.pop("stage"), kw.pop("fmt")
     z3 = stage == 3
@@ -444,21 +489,56 @@ def test_native_executor_equals_call_by_call(mode):
     m0 = torch.from_numpy(c.master0(L))
     a.load_master(m0)
     b.load_master(m0)
-    b.timers = {}                       # the Python call-by-call sequencer
     for s in range(1, 4):
         reps = c.grads_torch(L, s, a.read_state()["loss_scale"])
         for r, g in enumerate(reps):
             a.grads[r].copy_(g.cuda())
             b.grads[r].copy_(g.cuda())
         a.step()
-        b.step()
+        _issue_step_calls(b)
     torch.cuda.synchronize()
-    assert b.timers and all(len(v) > 0 for v in b.timers.values())
     for name in ("master", "m", "v", "state"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
     assert torch.equal(a.shard16, b.shard16) if z3 else torch.equal(a.params, b.params)
     if mode == "z2_split_clip_fp16":
         assert a.read_state()["skipped"] == 1
+
+
+@pytest.mark.parametrize("live", [1, 2])
+def test_unit_hook_sees_every_gather_in_order(live):
+    # the executor's unit hook runs after each gather is issued, forward then backward, with the
+    # buffers that gather wrote; each holds the unit's previous parameters (the oracle's)
+    c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS)
+    L = c.layout()
+    eng = _engine(c, live_units=live)
+    m0 = c.master0(L)
+    eng.load_master(torch.from_numpy(m0))
+    zs = ZeroSimulation(L, m0, c.fmt, HP)
+    seen = []
+
+    def hook(kind, u, rows):
+        torch.cuda.current_stream().synchronize()
+        torch.cuda.synchronize()
+        seen.append((kind, u, rows[0].data_ptr(), [_u16(r[:L.units[u].real]) for r in rows]))
+
+    eng.transient_hook = hook
+    for s in (1, 2):
+        seen.clear()
+        prev = zs.flat("shard16")
+        reps = c.grads_torch(L, s, 1.0)
+        for r, g in enumerate(reps):
+            eng.grads[r].copy_(g.cuda())
+        eng.step()
+        zs.step([_u16(t) for t in reps])
+        U = len(L.units)
+        assert [(k, u) for k, u, _, _ in seen] == [("fwd", u) for u in range(U)] + \
+            [("bwd", u) for u in reversed(range(U))]
+        for k, u, _, rows in seen:
+            want = prev[L.units[u].offset:L.units[u].offset + L.units[u].real]
+            for row in rows:
+                assert np.array_equal(row, want), (k, u)
+        bufs = {p for _, _, p, _ in seen}
+        assert len(bufs) == live
 
 
 def test_launch_tracing_counts_every_call_of_the_executor():

@@ -89,6 +89,10 @@ class zero_trace_totals(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8), ("busy_ms", ctypes.c_double * 8)]
 
 
+ZERO_UNIT_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p)
+
+
 class zero_step_args(ctypes.Structure):
     _fields_ = [("hp", ctypes.POINTER(zero_adamw_hp)), ("max_norm", ctypes.c_double),
                 ("fused", ctypes.c_int32), ("per_bucket", ctypes.c_int32)] + \
@@ -96,7 +100,8 @@ class zero_step_args(ctypes.Structure):
                 ("grad_replicas", "master", "m", "v", "grad_shards", "param16_full", "param16_shards",
                  "transient")] + \
                [("state", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("transient2", ctypes.POINTER(ctypes.c_void_p))]
+                ("transient2", ctypes.POINTER(ctypes.c_void_p)), ("unit_hook", ZERO_UNIT_HOOK),
+                ("hook_user", ctypes.c_void_p)]
 
 
 class StepArgs:
@@ -117,6 +122,24 @@ class StepArgs:
             if arr is not None:
                 self._keep.append(arr)
                 setattr(self.args, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
+        self._n_d = L.n_d
+        self._hook = None
+
+    def set_unit_hook(self, fn) -> None:
+        """fn(pass_, unit, transient_addresses, stream_handle) or None: called
+        by the executor after it issues each ZeRO-3 unit gather (pass_ 0:
+        forward, 1: backward)."""
+        if fn is None:
+            self._hook = None
+            self.args.unit_hook = ZERO_UNIT_HOOK()
+            return
+        n_d = self._n_d
+
+        def trampoline(user, pass_, unit, transient, stream):
+            fn(int(pass_), int(unit), [transient[i] for i in range(n_d)], stream)
+
+        self._hook = ZERO_UNIT_HOOK(trampoline)
+        self.args.unit_hook = self._hook
 
 
 assert ctypes.sizeof(zero_step_state) == 96

@@ -81,6 +81,7 @@ zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const ch
     if ((rc = check_ptrs((const void* const*)a->param16_shards, n, w + " param16_shards")) != ZERO_OK) return rc;
     if ((rc = check_ptrs((const void* const*)a->transient, n, w + " transient")) != ZERO_OK) return rc;
     if (a->transient2 && L->stage != 3) return fail(ZERO_ERR_INVALID, w + ": transient2 is for ZeRO-3 only");
+    if (a->unit_hook && L->stage != 3) return fail(ZERO_ERR_INVALID, w + ": unit_hook is for ZeRO-3 only");
     if ((rc = check_ptrs((const void* const*)a->transient2, n, w + " transient2")) != ZERO_OK) return rc;
     const void* one[2] = {a->state, a->workspace};
     if (!a->state || !a->workspace) return fail(ZERO_ERR_INVALID, w + ": NULL state or workspace");
@@ -268,6 +269,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                      return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, buf, zst);
                  })) != ZERO_OK)
                 return rc;
+            if (a->unit_hook) a->unit_hook(a->hook_user, 0, u, buf, zst);
         }
         if (two) {  // forward reads of every unit end before any update rewrites a shard
             if ((rc = fork.join()) != ZERO_OK) return rc;
@@ -282,6 +284,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                      return zero_stage3_gather_layer(L, u, (const void* const*)a->param16_shards, buf, zst);
                  })) != ZERO_OK)
                 return rc;
+            if (a->unit_hook) a->unit_hook(a->hook_user, 1, u, buf, zst);
             if ((rc = ready(u, st)) != ZERO_OK) return rc;
             if (a->fused)
                 rc = traced(ZERO_CALL_FUSED_STEP, st, [&] {

@@ -20,10 +20,10 @@ library calls in the order the pages give:
   reading notes §3.1 and §4.3, "ZeRO-3 核心流程" §2).  With clipping or a scaler
   the shard updates wait for the global decision.
 
-The same calls can also be issued one by one from here (``_step``), for a
-per-call hook on the ZeRO-3 transients or per-call timers; results are
-identical.  Every arithmetic step runs inside libzero's kernels; this module
-only owns memory, orders calls and reads back the 96-byte step state.
+Gradient accumulation (``micro_step``) and the ZeRO-3 prefetch under a
+caller's compute (``step_overlapped``) issue their calls from here.  Every
+arithmetic step runs inside libzero's kernels; this module only owns memory,
+orders calls and reads back the 96-byte step state.
 """
 from __future__ import annotations
 
@@ -119,7 +119,7 @@ class ZeroStep:
         self._rows()
         self.hp = B.zero_adamw_hp(lr=adamw.lr, eps=adamw.eps, weight_decay=adamw.weight_decay)
         self.transient_hook = None  # called as hook(kind, unit, transient_rows) after each ZeRO-3 gather
-        self.timers = None          # dict: call name -> list of (start, end) CUDA events, when timing
+        self.timers = None          # micro_step: dict call name -> list of (start, end) CUDA events
         self.reset_state()
 
     def set_bucket_elems(self, bucket_elems: int) -> None:
@@ -193,9 +193,11 @@ class ZeroStep:
     def step_args(self) -> B.StepArgs:
         """This engine's buffers and settings as the library's zero_step_args
         (built once, as the buffers never move; built again if ``hp`` is
-        replaced by another object)."""
+        replaced by another object), with ``transient_hook`` installed as the
+        executor's unit hook."""
         if getattr(self, "_args", None) is None or self._args_hp is not self.hp:
             self._args_hp = self.hp
+            self._args_hook = None
             stage3 = self.stage == 3
             self._args = B.StepArgs(
                 self.L, self.hp, self.max_norm if not self.fused else 0.0, self.fused, self.per_bucket,
@@ -204,70 +206,27 @@ class ZeroStep:
                 self.shard16_rows if (stage3 or not self.fuse_allgather) else None,
                 self.transient_rows if stage3 else None, self.state, self.workspace,
                 self.transient2_rows if stage3 else None)
+        if self._args_hook is not self.transient_hook:
+            self._args_hook = self.transient_hook
+            self._args.set_unit_hook(self._unit_hook if self.transient_hook is not None else None)
         return self._args
 
-    def step(self) -> None:
-        """One step.  The library's step executor (zero_step) issues the
-        calls; with per-call timers or a transient hook set, the same calls
-        are issued from here instead, one by one."""
-        if self.timers is None and self.transient_hook is None:
-            B.zero_step(self.L, self.step_args(), self._s())
-        else:
-            self._step(self.per_bucket)
+    def _unit_hook(self, pass_: int, unit: int, addresses, stream) -> None:
+        """The executor's unit hook: hand the gathered unit's transient rows to
+        ``transient_hook(kind, unit, rows)``."""
+        first = addresses[0]
+        buf = self.transient
+        if self.transient2 is not None and first == self.transient2[0].data_ptr():
+            buf = self.transient2
+        self.transient_hook("fwd" if pass_ == 0 else "bwd", unit, [buf[r] for r in range(self.n_d)])
 
-    def _step(self, per_bucket: bool) -> None:
-        """The step's calls issued one by one, in zero_step's order, so that
-        each can be timed (``timers``) or followed by the transient hook."""
-        s = self._s()
-        L, C = self.L, self._call
-        if self.stage == 3:
-            U = len(self.units)
-            for u in range(U):                                   # forward
-                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
-                if self.transient_hook:
-                    self.transient_hook("fwd", u, self.transient_rows)
-            for u in reversed(range(U)):                         # backward
-                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
-                if self.transient_hook:
-                    self.transient_hook("bwd", u, self.transient_rows)
-                if self.fused:
-                    C("fused_step", B.zero_fused_step, L, u, self.hp, self.grad_rows, self.master_rows,
-                      self.m_rows, self.v_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS,
-                      self.workspace, s)
-                else:
-                    C("reduce_scatter", B.zero_reduce_scatter, L, u, self.grad_rows, self.gshard_rows,
-                      self.state, self.workspace, s)
-            if self.fused:
-                C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
-            else:
-                C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state,
-                  self.workspace, s)
-                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
-                  self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
-            return
-        if self.fused:
-            if per_bucket:
-                for b in reversed(range(self.n_buckets)):
-                    C("fused_step", B.zero_fused_step, L, b, self.hp, self.grad_rows, self.master_rows,
-                      self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
-                      self.workspace, s)
-            else:
-                C("fused_step", B.zero_fused_step, L, -1, self.hp, self.grad_rows, self.master_rows,
-                  self.m_rows, self.v_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS,
-                  self.workspace, s)
-            C("grad_norm", B.zero_grad_norm, L, 0.0, B.ZERO_NORM_AFTER_FUSED, self.state, self.workspace, s)
-        else:
-            for b in reversed(range(self.n_buckets)):
-                C("reduce_scatter", B.zero_reduce_scatter, L, b, self.grad_rows, self.gshard_rows, self.state,
-                  self.workspace, s)
-            C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
-            if self.fuse_allgather:
-                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
-                  self.gshard_rows, self.state, self.param_rows, B.ZERO_OUT_FULL_REPLICAS, s)
-            else:
-                C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
-                  self.gshard_rows, self.state, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
-                C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
+    def step(self) -> None:
+        """One step: one call of the library's step executor (zero_step), which
+        issues the step's calls in the pages' order (see ``zero.h``).  A
+        ``transient_hook(kind, unit, rows)`` set on the engine is called after
+        each ZeRO-3 unit gather is issued, where a layer's compute would be
+        enqueued."""
+        B.zero_step(self.L, self.step_args(), self._s())
 
     # -- ZeRO-3 prefetch: gathers on a second stream overlap the layers' compute -------
     def step_overlapped(self, compute, max_live_units: int = 2, comm_ctas: int = 0) -> None:
