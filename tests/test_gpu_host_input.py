@@ -71,3 +71,28 @@ def test_host_state_read_back_in_the_call():
         torch.cuda.current_stream().synchronize()
         assert torch.equal(out, eng.state.cpu())
         assert eng.read_state()["t"] == s
+
+
+def test_host_input_from_pageable_memory_through_the_c_call():
+    # zero_step_from_host accepts pageable host memory too (the copies then stage through the
+    # driver); results equal the device-resident step bit for bit
+    from zero_partitioned_mixed_replica_gb300 import binding as B
+    from tests.test_gpu_parity import _engine
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=32_768, max_norm=0.05)
+    L = c.layout()
+    a, b = _engine(c), _engine(c)
+    m0 = torch.from_numpy(c.master0(L))
+    a.load_master(m0)
+    b.load_master(m0)
+    state = torch.zeros(96, dtype=torch.uint8)              # pageable as well
+    for s in (1, 2):
+        reps = c.grads_torch(L, s, 1.0)
+        host = torch.stack(reps)                            # pageable CPU tensor, N_d x Psi_pad
+        B.zero_step_from_host(a.L, a.step_args(), [host[r] for r in range(c.n_d)], 10_000, state)
+        for r, g in enumerate(reps):
+            b.grads[r].copy_(g.cuda())
+        b.step()
+        torch.cuda.synchronize()
+        assert torch.equal(state, a.state.cpu())
+    for name in ("master", "m", "v", "params", "state"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name

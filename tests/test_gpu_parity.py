@@ -599,3 +599,33 @@ def test_single_parameter_buffers(n_d, stage, fmt, max_norm):
     if max_norm > 0:    # the coefficients agree to one binary32 rounding (the norm's partial, above)
         assert all(0 < g["clip_coef"] <= 1 and abs(g["clip_coef"] - o["clip"]) <= 2.0 ** -23 * o["clip"]
                    for g, o in hist if not g["overflow"])
+
+
+def test_tracing_is_off_inside_a_graph_capture():
+    # traced calls record no events while their stream is being captured; the replayed graph
+    # equals eager steps, and tracing resumes for eager calls afterwards
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    c = Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=4096)    # 43 buckets: two streams
+    L = c.layout()
+    a, b = _engine(c), _engine(c)
+    for e in (a, b):
+        e.load_master(torch.from_numpy(c.master0(L)))
+        for r, g in enumerate(c.grads_torch(L, 1, 1.0)):
+            e.grads[r].copy_(g.cuda())
+    Bd.zero_trace_read(reset=True)
+    prev = Bd.zero_trace_enable(True)
+    try:
+        graph = a.capture()
+        assert Bd.zero_trace_read(reset=True) == {}
+        a.reset_state()
+        a.load_master(torch.from_numpy(c.master0(L)))
+        for _ in range(2):
+            graph.replay()
+            b.step()
+        torch.cuda.synchronize()
+        t = Bd.zero_trace_read(reset=True)
+        assert t["fused_step"]["launches"] == 2 * b.n_buckets        # the eager steps only
+    finally:
+        Bd.zero_trace_enable(prev)
+    for name in ("master", "m", "v", "params"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
