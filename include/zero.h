@@ -394,14 +394,14 @@ typedef struct zero_step_args {
  *     u = U-1..0: gather u again and zero_fused_step(u) (fused) or
  *     zero_reduce_scatter(u) (split, followed by the norm and the shard
  *     update after the loop).  With transient2, units alternate between the
- *     two buffer sets and between `stream` and the library's second stream;
+ *     two buffer sets and between `stream` and one of the library's streams;
  *     every forward gather ends before the first update.
  * ZeRO-1/2 bucket launches of short buckets (mean at most 2^27 elements)
- * alternate between `stream` and a second stream of the library's (one per
- * device, created at the first call), which joins `stream` again before the
- * norm: consecutive buckets touch disjoint elements
- * and norm-partial slots, so one bucket's launch can start while the previous
- * one drains.  Results do not depend on it.
+ * rotate over `stream` and three streams of the library's (created per device
+ * at the first call), which join `stream` again before the norm: consecutive
+ * buckets touch disjoint elements and norm-partial slots, so one bucket's
+ * launch can start while the previous one drains.  Results do not depend on
+ * it.
  * Asynchronous on `stream`; allocates no device memory; captures into a CUDA
  * graph like the calls it issues.  Calls on one device are serialised by a
  * library lock.  Errors: those of the calls it issues (the first failing call

@@ -237,3 +237,28 @@ def test_ctypes_structs_match_the_header(tmp_path):
         assert int(got[name]) == ctypes.sizeof(cls), name
         for f in cls._fields_:
             assert int(got["%s.%s" % (name, f[0])]) == getattr(cls, f[0]).offset, (name, f[0])
+
+
+def test_unit_hook_trampoline_keeps_the_first_exception():
+    # the executor calls the hook through a C function pointer; an exception cannot cross the C
+    # frames, so the binding keeps the first one and re-raises it after the call
+    L3 = B.zero_layout_init([1000, 24], [0, 1], 2, 3, 0, 0, B.ZERO_BF16)
+    hp = B.zero_adamw_hp(lr=1e-3, eps=1e-8, weight_decay=0.0)
+    two = [FAKE, FAKE]
+    a = B.StepArgs(L3, hp, 0.0, True, True, two, two, two, two, None, None, two, two, FAKE, FAKE)
+    seen = []
+
+    def hook(pass_, unit, addresses, stream):
+        seen.append((pass_, unit, addresses))
+        raise KeyError("planted")
+
+    a.set_unit_hook(hook)
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE + 256)
+    for unit in (0, 1):          # call the C function pointer the way the executor does
+        a.args.unit_hook(None, 0, unit, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), None)
+    assert seen == [(0, 0, [FAKE, FAKE + 256])]      # the second call is skipped after the error
+    with pytest.raises(KeyError, match="planted"):
+        B._raise_hook_error(a)
+    B._raise_hook_error(a)                              # cleared once raised
+    a.set_unit_hook(None)
+    assert not a.args.unit_hook

@@ -629,3 +629,23 @@ def test_tracing_is_off_inside_a_graph_capture():
         Bd.zero_trace_enable(prev)
     for name in ("master", "m", "v", "params"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def test_unit_hook_exceptions_reach_the_caller():
+    # an exception cannot cross the executor's C frames; the binding re-raises the hook's first one
+    c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS)
+    eng = _engine(c)
+    calls = []
+
+    def hook(kind, u, rows):
+        calls.append((kind, u))
+        if (kind, u) == ("fwd", 1):
+            raise ValueError("planted in the hook")
+
+    eng.transient_hook = hook
+    with pytest.raises(ValueError, match="planted in the hook"):
+        eng.step()
+    assert calls[:2] == [("fwd", 0), ("fwd", 1)] and len(calls) == 2     # later calls are skipped
+    eng.transient_hook = None
+    eng.step()                                                            # the engine stays usable
+    assert eng.read_state()["error"] == 0

@@ -124,6 +124,7 @@ class StepArgs:
                 setattr(self.args, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
         self._n_d = L.n_d
         self._hook = None
+        self.hook_error = None      # first exception raised by the unit hook during a call
 
     def set_unit_hook(self, fn) -> None:
         """fn(pass_, unit, transient_addresses, stream_handle) or None: called
@@ -136,7 +137,13 @@ class StepArgs:
         n_d = self._n_d
 
         def trampoline(user, pass_, unit, transient, stream):
-            fn(int(pass_), int(unit), [transient[i] for i in range(n_d)], stream)
+            # an exception cannot cross the C frames: keep the first one for the caller to re-raise
+            if self.hook_error is not None:
+                return
+            try:
+                fn(int(pass_), int(unit), [transient[i] for i in range(n_d)], stream)
+            except BaseException as ex:     # noqa: BLE001 (re-raised by zero_step)
+                self.hook_error = ex
 
         self._hook = ZERO_UNIT_HOOK(trampoline)
         self.args.unit_hook = self._hook
@@ -368,16 +375,30 @@ def zero_reduce_scatter_micro(L: Layout, bucket_or_unit: int, micro: int, n_micr
                                            _ptrs(acc_shards, L), _addr(st), _addr(workspace), _stream(stream)))
 
 
+def _raise_hook_error(args: StepArgs) -> None:
+    ex, args.hook_error = args.hook_error, None
+    if ex is not None:
+        raise ex
+
+
 def zero_step(L: Layout, args: StepArgs, stream=None) -> None:
-    _check(lib().zero_step(L, ctypes.byref(args.args), _stream(stream)))
+    """One step; an exception raised by the unit hook is re-raised here,
+    after the call (the executor has issued the whole step by then)."""
+    args.hook_error = None
+    status = lib().zero_step(L, ctypes.byref(args.args), _stream(stream))
+    _raise_hook_error(args)
+    _check(status)
 
 
 def zero_step_from_host(L: Layout, args: StepArgs, host_grads, chunk_elems: int = 0, host_state=None,
                         stream=None) -> None:
     """host_grads: one host pointer (or CPU tensor) per rank; host_state: a
     CPU tensor / address of 96 bytes, or None."""
-    _check(lib().zero_step_from_host(L, ctypes.byref(args.args), _ptrs(host_grads, L), int(chunk_elems),
-                                     _addr(host_state), _stream(stream)))
+    args.hook_error = None
+    status = lib().zero_step_from_host(L, ctypes.byref(args.args), _ptrs(host_grads, L), int(chunk_elems),
+                                       _addr(host_state), _stream(stream))
+    _raise_hook_error(args)
+    _check(status)
 
 
 def zero_trace_enable(on: bool) -> bool:

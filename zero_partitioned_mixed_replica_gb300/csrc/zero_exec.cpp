@@ -143,14 +143,24 @@ zero_status_t traced(int32_t kind, cudaStream_t st, Call&& call) {
 
 // ---------------------------------------------------------------------------
 // Per-device resources of the executor, created at first use and kept until
-// the process exits: a second stream for alternating bucket launches with its
+// the process exits: the extra streams that bucket launches rotate over, with their
 // fork/join events, and the host-input copy streams with their events.  One
 // lock per device serialises the calls that use them.
 // ---------------------------------------------------------------------------
+// Streams that short bucket launches rotate over (the caller's plus
+// kLanes - 1 of the library's).  GB300, GPT-2 small ZeRO-1, 25 buckets of
+// 5M elements, ms per step eager / from a CUDA graph: 2 lanes 1.081 / 1.074,
+// 3 lanes 1.065 / 1.052, 4 lanes 1.054 / 1.051.
+#ifndef ZK_BUCKET_LANES
+#define ZK_BUCKET_LANES 4
+#endif
+constexpr int kLanes = ZK_BUCKET_LANES;
+static_assert(kLanes >= 2, "the executor needs a second stream");
+
 struct DeviceRes {
     std::mutex mu;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t aux[kLanes - 1] = {};
+    cudaEvent_t fork = nullptr, join[kLanes - 1] = {};
     cudaStream_t cs[2] = {nullptr, nullptr};
     cudaEvent_t start = nullptr;
     std::vector<cudaEvent_t> ev;  // two per bucket: one per copy stream
@@ -180,9 +190,11 @@ zero_status_t make_event(cudaEvent_t* ev, const char* what) {
 
 zero_status_t step_res(DeviceRes& R, const char* what) {
     zero_status_t rc;
-    if ((rc = make_stream(&R.aux, what)) != ZERO_OK) return rc;
-    if ((rc = make_event(&R.fork, what)) != ZERO_OK) return rc;
-    return make_event(&R.join, what);
+    for (int i = 0; i < kLanes - 1; ++i) {
+        if ((rc = make_stream(&R.aux[i], what)) != ZERO_OK) return rc;
+        if ((rc = make_event(&R.join[i], what)) != ZERO_OK) return rc;
+    }
+    return make_event(&R.fork, what);
 }
 
 zero_status_t wait_on(cudaStream_t waiter, cudaEvent_t ev, cudaStream_t recorder, const char* what) {
@@ -191,25 +203,32 @@ zero_status_t wait_on(cudaStream_t waiter, cudaEvent_t ev, cudaStream_t recorder
     return e == cudaSuccess ? ZERO_OK : cuda_fail(what, e);
 }
 
-// The device's second stream, forked from `s` (it waits for the work queued
-// on `s`) and joined back (`s` waits for it) explicitly or, if a call of the
+// The device's extra streams, forked from `s` (they wait for the work queued
+// on `s`) and joined back (`s` waits for them) explicitly or, if a call of the
 // step fails in between, when the fork goes out of scope: the caller's
-// stream never runs ahead of work left on the second stream.
+// stream never runs ahead of work left on the extra streams.
 class Fork {
   public:
     Fork(cudaStream_t s, DeviceRes& R) : s_(s), R_(R) {}
     zero_status_t open() {
-        zero_status_t rc = wait_on(R_.aux, R_.fork, s_, "zero_step: fork");
-        open_ = rc == ZERO_OK;
-        return rc;
+        cudaError_t e = cudaEventRecord(R_.fork, s_);
+        for (int i = 0; e == cudaSuccess && i < kLanes - 1; ++i) e = cudaStreamWaitEvent(R_.aux[i], R_.fork, 0);
+        open_ = e == cudaSuccess;
+        return open_ ? ZERO_OK : cuda_fail("zero_step: fork", e);
     }
     zero_status_t join() {
         if (!open_) return ZERO_OK;
         open_ = false;
-        return wait_on(s_, R_.join, R_.aux, "zero_step: join");
+        for (int i = 0; i < kLanes - 1; ++i) {
+            zero_status_t rc = wait_on(s_, R_.join[i], R_.aux[i], "zero_step: join");
+            if (rc != ZERO_OK) return rc;
+        }
+        return ZERO_OK;
     }
     ~Fork() {  // after a failed call: join without replacing that call's error message
-        if (open_ && cudaEventRecord(R_.join, R_.aux) == cudaSuccess) cudaStreamWaitEvent(s_, R_.join, 0);
+        if (!open_) return;
+        for (int i = 0; i < kLanes - 1; ++i)
+            if (cudaEventRecord(R_.join[i], R_.aux[i]) == cudaSuccess) cudaStreamWaitEvent(s_, R_.join[i], 0);
     }
 
   private:
@@ -220,8 +239,8 @@ class Fork {
 
 using Ready = std::function<zero_status_t(int32_t, cudaStream_t)>;
 
-// Mean bucket length up to which consecutive bucket launches alternate
-// between two streams.  GB300, 350M layout, fused step: alternating raised
+// Mean bucket length up to which consecutive bucket launches rotate over
+// several streams.  GB300, 350M layout, fused step: alternating raised
 // every bucket size measured, 1e5 to 5e7 elements (5e7 at N_d = 2: 6.11 TB/s
 // on one stream, 8 buckets); the 1.5B run's 500M-element buckets drain in
 // about 0.1% of a launch and stay on one stream.
@@ -232,11 +251,10 @@ constexpr int64_t kAlternateMaxElems = (int64_t)1 << 27;
 // that call is issued on.
 //
 // Consecutive bucket launches of ZeRO-1/2 touch disjoint elements and write
-// their norm partials to fixed, disjoint slots, so short ones alternate
-// between `s` and the device's second stream: the next bucket's CTAs start on
-// the SMs that the previous bucket's last CTAs free, instead of after its
-// whole grid has drained.  The second stream joins `s` before the global
-// norm.  Results do not depend on it (every output element and partial has
+// their norm partials to fixed, disjoint slots, so short ones rotate over `s`
+// and the device's extra streams: the next bucket's CTAs start on the SMs
+// that the previous bucket's last CTAs free, instead of after its whole grid
+// has drained.  The extra streams join `s` before the global norm.  Results do not depend on it (every output element and partial has
 // one writer).
 zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
                        const Ready& ready) {
@@ -255,7 +273,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
         const bool two = a->transient2 != nullptr && U > 1;
         auto lane = [&](int32_t i, cudaStream_t& st, void* const*& buf) {
             const bool odd = two && (i & 1);
-            st = odd ? R.aux : s;
+            st = odd ? R.aux[0] : s;
             buf = odd ? a->transient2 : a->transient;
         };
         Fork fork(s, R);
@@ -321,13 +339,14 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
              })) != ZERO_OK)
             return rc;
     } else {
-        // alternate only short buckets: a launch's ramp and drain cost a few
+        // rotate only short buckets: a launch's ramp and drain cost a few
         // microseconds, which matters at 5M-50M elements per bucket, not at 500M
         const bool two = nb > 1 && L->psi_pad / nb <= kAlternateMaxElems;
         Fork fork(s, R);
         if (two && (rc = fork.open()) != ZERO_OK) return rc;
         for (int32_t b = nb - 1, i = 0; b >= 0; --b, ++i) {  // last bucket first
-            const cudaStream_t sb = (two && (i & 1)) ? R.aux : s;
+            const int lane = two ? i % kLanes : 0;
+            const cudaStream_t sb = lane ? R.aux[lane - 1] : s;
             const zero_stream_t zb = reinterpret_cast<zero_stream_t>(sb);
             if ((rc = ready(b, sb)) != ZERO_OK) return rc;
             if (a->fused)
