@@ -240,10 +240,10 @@ class Fork {
 using Ready = std::function<zero_status_t(int32_t, cudaStream_t)>;
 
 // Mean bucket length up to which consecutive bucket launches rotate over
-// several streams.  GB300, 350M layout, fused step: alternating raised
-// every bucket size measured, 1e5 to 5e7 elements (5e7 at N_d = 2: 6.11 TB/s
-// on one stream, 8 buckets); the 1.5B run's 500M-element buckets drain in
-// about 0.1% of a launch and stay on one stream.
+// several streams.  GB300, 350M layout, fused step: rotating raised every
+// bucket size measured, 1e5 to 5e7 elements (5e7 at N_d = 2, 8 buckets: 6.11
+// TB/s on one stream, 6.37 rotated); the 1.5B run's 500M-element buckets
+// drain in about 0.1% of a launch and stay on one stream.
 constexpr int64_t kAlternateMaxElems = (int64_t)1 << 27;
 
 // The step's calls on `s`.  ready(k, stream) runs before the first call that
@@ -253,9 +253,10 @@ constexpr int64_t kAlternateMaxElems = (int64_t)1 << 27;
 // Consecutive bucket launches of ZeRO-1/2 touch disjoint elements and write
 // their norm partials to fixed, disjoint slots, so short ones rotate over `s`
 // and the device's extra streams: the next bucket's CTAs start on the SMs
-// that the previous bucket's last CTAs free, instead of after its whole grid
-// has drained.  The extra streams join `s` before the global norm.  Results do not depend on it (every output element and partial has
-// one writer).
+// that the previous buckets' last CTAs free, instead of after their grids
+// have drained.  The extra streams join `s` before the global norm.  Results
+// do not depend on the rotation: every output element and partial has one
+// writer.
 zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
                        const Ready& ready) {
     zero_status_t rc;
@@ -267,7 +268,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
         // buffers and streams, so a unit's gather runs while the previous
         // unit's reduce-scatter and update drain.  A unit's gather and its
         // update stay on one stream (the update rewrites the 16-bit shard the
-        // gather reads); units sharing a buffer share a stream; the second
+        // gather reads); units sharing a buffer share a stream; the extra
         // stream joins `s` after the forward gathers and again before the norm.
         const int32_t U = (int32_t)L->segs.size();
         const bool two = a->transient2 != nullptr && U > 1;
