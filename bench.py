@@ -395,7 +395,7 @@ def gpu_run(args, w, rank, world, local_rank):
         run = (lambda: graph.replay()) if graph is not None else eng.step
     # the warm-up steps run traced too, so that the timed steps reuse the trace's events
     # instead of creating them inside the timed region
-    trace = graph is None and args.micro == 1
+    trace = graph is None
     B.zero_trace_enable(trace)
     for _ in range(args.warmup):
         run()
@@ -413,10 +413,7 @@ def gpu_run(args, w, rank, world, local_rank):
     clocks = ClockSampler(uuid)
     time.sleep(0.3)
     # per-call durations from CUDA events on each call's launching stream: the library's
-    # launch tracing for the step executor (zero_step); the engine's own per-call events
-    # for the micro-batch calls it issues itself
-    if graph is None and args.micro > 1:
-        eng.timers = {}
+    # launch tracing of the step executor (zero_step, zero_micro_step)
     if trace:
         B.zero_trace_enable(True)
     B.zero_launch_count(reset=True)
@@ -431,7 +428,6 @@ def gpu_run(args, w, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
-    timers, eng.timers = eng.timers, None
     traced = None
     if trace:
         B.zero_trace_enable(False)
@@ -446,13 +442,7 @@ def gpu_run(args, w, rank, world, local_rank):
     st = eng.read_state()
 
     # --- per-kernel averages from events on the launching stream ------------------
-    kern = {}
-    if traced:
-        kern = traced
-    elif timers:
-        for name, evs in timers.items():
-            d = [a.elapsed_time(b) for a, b in evs]
-            kern[name] = {"launches": len(d), "total_ms": sum(d), "avg_ms": sum(d) / len(d)}
+    kern = traced or {}
     # --- e2e: host buffers, H2D of the step's gradients + D2H of the step result ----
     e2e = None
     need = int(eng.grads.numel() * eng.grads.element_size())

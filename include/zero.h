@@ -431,7 +431,7 @@ zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* ar
                                   const void* const* host_grads, int64_t chunk_elems, void* host_state,
                                   zero_stream_t stream);
 
-/* Launch tracing of zero_step and zero_step_from_host.  With tracing on,
+/* Launch tracing of zero_step, zero_micro_step and zero_step_from_host.  With tracing on,
  * every library call the executor issues is bracketed by two timing events
  * recorded on the stream the call is issued on (none while that stream is
  * being captured into a CUDA graph); zero_trace_read waits for the recorded
@@ -444,7 +444,8 @@ enum {
     ZERO_CALL_FUSED_STEP = 3,
     ZERO_CALL_STAGE3_GATHER = 4,
     ZERO_CALL_ALLGATHER = 5,
-    ZERO_CALL_KINDS = 6
+    ZERO_CALL_ACCUMULATE = 6,
+    ZERO_CALL_KINDS = 7
 };
 typedef struct zero_trace_totals {
     int64_t calls[8];             /* traced calls per ZERO_CALL_* kind          */
@@ -501,6 +502,25 @@ zero_status_t zero_reduce_scatter_accumulated(const zero_layout* L, int32_t buck
 zero_status_t zero_reduce_scatter_micro(const zero_layout* L, int32_t bucket_or_unit, int32_t micro,
                                         int32_t n_micro, const void* const* grad_replicas, float* const* acc_shards,
                                         zero_step_state* st, void* workspace, zero_stream_t stream);
+
+/* Micro-batch `micro` (0-based) of an optimizer step over n_micro
+ * micro-batches, whose 16-bit gradients are in args->grad_replicas, issued
+ * by the step executor with the calls above ([RN] §4.1-§4.3):
+ *   ZeRO-1: zero_accumulate_grads into acc_replicas (N_d fp32 buffers of
+ *     Psi_pad); the last micro-batch then reduce-scatters the accumulators
+ *     bucket by bucket (zero_reduce_scatter_accumulated);
+ *   ZeRO-2: zero_reduce_scatter_micro for every bucket, every micro-batch;
+ *   ZeRO-3: every unit gathered forward and backward and reduced
+ *     (zero_reduce_scatter_micro) every micro-batch;
+ * and after the last micro-batch's reductions zero_grad_norm(DECIDE) and the
+ * update, as zero_step's split step.  Requires args->fused = 0 when
+ * n_micro > 1; n_micro = 1 is zero_step.  Bucket launches rotate over streams
+ * and ZeRO-3 units use transient2 as in zero_step.  acc_replicas: ZeRO-1 with
+ * n_micro > 1 only (else ignored).  Errors: micro out of [0, n_micro),
+ * fused with n_micro > 1, missing accumulators (ZERO_ERR_INVALID), and those
+ * of zero_step. */
+zero_status_t zero_micro_step(const zero_layout* L, const zero_step_args* args, int32_t micro, int32_t n_micro,
+                              float* const* acc_replicas, zero_stream_t stream);
 
 /* Largest Psi_pad that zero_fused_step_noalloc accepts (64 Mi elements). */
 #define ZERO_NOALLOC_MAX_ELEMS 67108864

@@ -209,6 +209,12 @@ def test_executor_and_cast_validate_before_launch():
     assert status(B.zero_step_from_host, L, args(L, False, full=[FAKE, MIS]), two, 0, None, 0) == B.ZERO_ERR_ALIGN
     assert B.lib().zero_trace_read(None, 0) == B.ZERO_ERR_INVALID
     assert B.zero_trace_read() == {}             # nothing traced: no kind reported
+    L1 = B.zero_layout_init([1000, 24], None, 2, 1, 0, 0, B.ZERO_BF16)
+    assert status(B.zero_micro_step, L, args(L, False), 2, 2, None, 0) == B.ZERO_ERR_INVALID      # micro >= n_micro
+    assert status(B.zero_micro_step, L, args(L, False), -1, 2, None, 0) == B.ZERO_ERR_INVALID
+    assert status(B.zero_micro_step, L, args(L, True, gshard=None), 0, 2, None, 0) == B.ZERO_ERR_INVALID  # fused
+    assert status(B.zero_micro_step, L1, args(L1, False), 0, 2, None, 0) == B.ZERO_ERR_INVALID    # no accumulators
+    assert status(B.zero_micro_step, L1, args(L1, False), 0, 2, [FAKE, MIS], 0) == B.ZERO_ERR_ALIGN
     assert status(B.zero_cast_params, L3, two, two, B.ZERO_OUT_FULL_REPLICAS, 0) == B.ZERO_ERR_STATE
     assert status(B.zero_cast_params, L, two, two, 5, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_cast_params, L, [FAKE, MIS], two, B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_ALIGN

@@ -25,12 +25,12 @@ def _u16(t):
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _run(c: Case, M: int, steps: int, use_gpu_clip: bool = False):
+def _run(c: Case, M: int, steps: int, use_gpu_clip: bool = False, live_units: int = 1):
     from zero_partitioned_mixed_replica_gb300.engine import AdamW, ZeroStep
     L = c.layout()
     eng = ZeroStep(c.numels, c.n_d, c.stage, c.fmt, c.bucket_elems, c.units,
                    AdamW(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay), c.max_norm, c.loss_scale,
-                   c.dynamic, c.growth_interval, n_micro=M)
+                   c.dynamic, c.growth_interval, n_micro=M, live_units=live_units)
     m0 = c.master0(L)
     eng.load_master(torch.from_numpy(m0))
     zs = ZeroSimulation(L, m0, c.fmt, HP, max_norm=c.max_norm, loss_scale=c.loss_scale, dynamic=c.dynamic,
@@ -82,8 +82,30 @@ def test_zero2_generic_rank_count():
     _run(Case(NUMELS, 5, 2, FMT_BF16, bucket_elems=32_768), M=2, steps=2)
 
 
-def test_zero3_accumulation():
-    _run(Case(NUMELS, 2, 3, FMT_BF16, units=[0, 1, 1, 2]), M=3, steps=2)
+@pytest.mark.parametrize("live", [1, 2])
+def test_zero3_accumulation(live):
+    _run(Case(NUMELS, 2, 3, FMT_BF16, units=[0, 1, 1, 2]), M=3, steps=2, live_units=live)
+
+
+def test_micro_steps_are_traced_per_call():
+    # zero_micro_step issues the accumulation's calls: ZeRO-1 accumulates every micro-batch and
+    # reduce-scatters once per bucket; ZeRO-2 reduce-scatters every bucket every micro-batch
+    from zero_partitioned_mixed_replica_gb300 import binding as B
+    for stage, M in ((1, 3), (2, 3)):
+        c = Case(NUMELS, 4, stage, FMT_BF16, bucket_elems=8192, max_norm=1.0)
+        B.zero_trace_read(reset=True)
+        prev = B.zero_trace_enable(True)
+        try:
+            eng = _run(c, M=M, steps=1)
+        finally:
+            B.zero_trace_enable(prev)
+        t = B.zero_trace_read(reset=True)
+        nb = eng.n_buckets
+        if stage == 1:
+            assert t["accumulate"]["launches"] == M and t["reduce_scatter"]["launches"] == nb
+        else:
+            assert "accumulate" not in t and t["reduce_scatter"]["launches"] == M * nb
+        assert t["grad_norm"]["launches"] == 1 and t["adamw"]["launches"] == 1
 
 
 def test_zero2_overflow_in_a_middle_micro_batch_skips_the_step():

@@ -38,7 +38,7 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_reduce_scatter", "zero_grad_norm", "zero_adamw_shard_step",
             "zero_allgather_params", "zero_cast_params", "zero_stage3_gather_layer", "zero_fused_step",
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
-            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_step_from_host",
+            "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_micro_step", "zero_step_from_host",
             "zero_trace_enable", "zero_trace_read", "zero_set_max_ctas",
             "zero_last_error", "zero_launch_count"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
@@ -82,7 +82,7 @@ class zero_adamw_hp(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
 
 
-ZERO_CALL_NAMES = ["reduce_scatter", "grad_norm", "adamw", "fused_step", "stage3_gather", "allgather"]
+ZERO_CALL_NAMES = ["reduce_scatter", "grad_norm", "adamw", "fused_step", "stage3_gather", "allgather", "accumulate"]
 
 
 class zero_trace_totals(ctypes.Structure):
@@ -186,6 +186,7 @@ def lib():
         "zero_reduce_scatter_micro": [P, i32, i32, i32, PP, PP, P, P, P],
         "zero_step": [P, ctypes.POINTER(zero_step_args), P],
         "zero_step_from_host": [P, ctypes.POINTER(zero_step_args), PP, i64, P, P],
+        "zero_micro_step": [P, ctypes.POINTER(zero_step_args), i32, i32, PP, P],
         "zero_trace_read": [ctypes.POINTER(zero_trace_totals), i32],
     }
     for name, args in sig.items():
@@ -386,6 +387,14 @@ def zero_step(L: Layout, args: StepArgs, stream=None) -> None:
     after the call (the executor has issued the whole step by then)."""
     args.hook_error = None
     status = lib().zero_step(L, ctypes.byref(args.args), _stream(stream))
+    _raise_hook_error(args)
+    _check(status)
+
+
+def zero_micro_step(L: Layout, args: StepArgs, micro: int, n_micro: int, acc_replicas=None, stream=None) -> None:
+    args.hook_error = None
+    status = lib().zero_micro_step(L, ctypes.byref(args.args), int(micro), int(n_micro),
+                                   _ptrs(acc_replicas, L), _stream(stream))
     _raise_hook_error(args)
     _check(status)
 

@@ -257,11 +257,37 @@ constexpr int64_t kAlternateMaxElems = (int64_t)1 << 27;
 // have drained.  The extra streams join `s` before the global norm.  Results
 // do not depend on the rotation: every output element and partial has one
 // writer.
+// Micro-batch `micro` of `n_micro` (n_micro = 1: the plain step).  Before
+// the last one the step stops after its reductions; ZeRO-1 only accumulates
+// locally (into `acc`) until the last one, which reduces the accumulators.
+struct Micro {
+    int32_t micro = 0, n_micro = 1;
+    float* const* acc = nullptr;
+    bool last() const { return micro == n_micro - 1; }
+};
+
 zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
-                       const Ready& ready) {
+                       const Ready& ready, const Micro& mb = Micro()) {
     zero_status_t rc;
     const int32_t nb = (int32_t)L->buckets.size();
     const zero_stream_t zs = reinterpret_cast<zero_stream_t>(s);
+    // the reduction of bucket (ZeRO-3: unit) k on stream `st`
+    auto reduce = [&](int32_t k, zero_stream_t st, void* const* out16, int32_t out_kind) -> zero_status_t {
+        if (a->fused)
+            return traced(ZERO_CALL_FUSED_STEP, reinterpret_cast<cudaStream_t>(st), [&] {
+                return zero_fused_step(L, k, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state, out16,
+                                       out_kind, a->workspace, st);
+            });
+        return traced(ZERO_CALL_REDUCE_SCATTER, reinterpret_cast<cudaStream_t>(st), [&] {
+            if (mb.n_micro == 1)
+                return zero_reduce_scatter(L, k, a->grad_replicas, a->grad_shards, a->state, a->workspace, st);
+            if (L->stage == 1)
+                return zero_reduce_scatter_accumulated(L, k, (const float* const*)mb.acc, a->grad_shards,
+                                                       mb.n_micro, a->state, a->workspace, st);
+            return zero_reduce_scatter_micro(L, k, mb.micro, mb.n_micro, a->grad_replicas, a->grad_shards, a->state,
+                                             a->workspace, st);
+        });
+    };
     if (L->stage == 3) {
         // One transient buffer: every unit on `s`.  Two (transient2): the
         // pages' prefetch with two live units -- consecutive units alternate
@@ -305,18 +331,10 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                 return rc;
             if (a->unit_hook) a->unit_hook(a->hook_user, 1, u, buf, zst);
             if ((rc = ready(u, st)) != ZERO_OK) return rc;
-            if (a->fused)
-                rc = traced(ZERO_CALL_FUSED_STEP, st, [&] {
-                    return zero_fused_step(L, u, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                           a->param16_shards, ZERO_OUT_SHARDS, a->workspace, zst);
-                });
-            else
-                rc = traced(ZERO_CALL_REDUCE_SCATTER, st, [&] {
-                    return zero_reduce_scatter(L, u, a->grad_replicas, a->grad_shards, a->state, a->workspace, zst);
-                });
-            if (rc != ZERO_OK) return rc;
+            if ((rc = reduce(u, zst, a->param16_shards, ZERO_OUT_SHARDS)) != ZERO_OK) return rc;
         }
         if ((rc = fork.join()) != ZERO_OK) return rc;
+        if (!mb.last()) return ZERO_OK;  // more micro-batches to reduce before the update
         if (a->fused)
             return traced(ZERO_CALL_GRAD_NORM, s, [&] {
                 return zero_grad_norm(L, 0.0, ZERO_NORM_AFTER_FUSED, a->state, a->workspace, zs);
@@ -329,6 +347,15 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             return zero_adamw_shard_step(L, a->hp, a->master, a->m, a->v, (const float* const*)a->grad_shards,
                                          a->state, a->param16_shards, ZERO_OUT_SHARDS, zs);
         });
+    }
+    if (mb.n_micro > 1 && L->stage == 1) {
+        // ZeRO-1 accumulates every rank's full gradient locally; only the last
+        // micro-batch communicates (reading notes §4.1)
+        if ((rc = traced(ZERO_CALL_ACCUMULATE, s, [&] {
+                 return zero_accumulate_grads(L, mb.micro, a->grad_replicas, mb.acc, zs);
+             })) != ZERO_OK)
+            return rc;
+        if (!mb.last()) return ZERO_OK;
     }
     const bool one_launch = a->fused && !a->per_bucket;
     if (one_launch) {
@@ -350,18 +377,10 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             const cudaStream_t sb = lane ? R.aux[lane - 1] : s;
             const zero_stream_t zb = reinterpret_cast<zero_stream_t>(sb);
             if ((rc = ready(b, sb)) != ZERO_OK) return rc;
-            if (a->fused)
-                rc = traced(ZERO_CALL_FUSED_STEP, sb, [&] {
-                    return zero_fused_step(L, b, a->hp, a->grad_replicas, a->master, a->m, a->v, a->state,
-                                           a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, zb);
-                });
-            else
-                rc = traced(ZERO_CALL_REDUCE_SCATTER, sb, [&] {
-                    return zero_reduce_scatter(L, b, a->grad_replicas, a->grad_shards, a->state, a->workspace, zb);
-                });
-            if (rc != ZERO_OK) return rc;
+            if ((rc = reduce(b, zb, a->param16_full, ZERO_OUT_FULL_REPLICAS)) != ZERO_OK) return rc;
         }
         if ((rc = fork.join()) != ZERO_OK) return rc;
+        if (!mb.last()) return ZERO_OK;  // ZeRO-2: more micro-batches before the update
     }
     if (a->fused)
         return traced(ZERO_CALL_GRAD_NORM, s, [&] {
@@ -398,6 +417,33 @@ extern "C" zero_status_t zero_step(const zero_layout* L, const zero_step_args* a
     if ((rc = step_res(*R, "zero_step")) != ZERO_OK) return rc;
     return run_step(L, a, reinterpret_cast<cudaStream_t>(stream), *R,
                     [](int32_t, cudaStream_t) { return ZERO_OK; });
+}
+
+extern "C" zero_status_t zero_micro_step(const zero_layout* L, const zero_step_args* a, int32_t micro,
+                                         int32_t n_micro, float* const* acc_replicas, zero_stream_t stream) {
+    clear_error();
+    const char* what = "zero_micro_step";
+    zero_status_t rc = check_args(L, a, what);
+    if (rc != ZERO_OK) return rc;
+    if (n_micro < 1 || micro < 0 || micro >= n_micro)
+        return fail(ZERO_ERR_INVALID, "zero_micro_step: need 0 <= micro < n_micro");
+    if (n_micro > 1 && a->fused)
+        return fail(ZERO_ERR_INVALID, "zero_micro_step: gradient accumulation uses the split step (fused = 0)");
+    if (n_micro > 1 && L->stage == 1) {
+        if (!acc_replicas) return fail(ZERO_ERR_INVALID, "zero_micro_step: ZeRO-1 needs acc_replicas");
+        if ((rc = check_ptrs((const void* const*)acc_replicas, L->n_d, "zero_micro_step acc_replicas")) != ZERO_OK)
+            return rc;
+    }
+    DeviceRes* R = nullptr;
+    if ((rc = current_res(&R, what)) != ZERO_OK) return rc;
+    std::lock_guard<std::mutex> lock(R->mu);
+    if ((rc = step_res(*R, what)) != ZERO_OK) return rc;
+    Micro mb;
+    mb.micro = micro;
+    mb.n_micro = n_micro;
+    mb.acc = acc_replicas;
+    return run_step(L, a, reinterpret_cast<cudaStream_t>(stream), *R,
+                    [](int32_t, cudaStream_t) { return ZERO_OK; }, mb);
 }
 
 extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_step_args* a,

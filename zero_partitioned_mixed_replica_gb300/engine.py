@@ -20,10 +20,11 @@ library calls in the order the pages give:
   reading notes §3.1 and §4.3, "ZeRO-3 核心流程" §2).  With clipping or a scaler
   the shard updates wait for the global decision.
 
-Gradient accumulation (``micro_step``) and the ZeRO-3 prefetch under a
-caller's compute (``step_overlapped``) issue their calls from here.  Every
-arithmetic step runs inside libzero's kernels; this module only owns memory,
-orders calls and reads back the 96-byte step state.
+Gradient accumulation (``micro_step``) is one ``zero_micro_step`` call per
+micro-batch.  Only the ZeRO-3 prefetch under a caller's compute
+(``step_overlapped``) issues its calls from here.  Every arithmetic step runs
+inside libzero's kernels; this module only owns memory, orders calls and
+reads back the 96-byte step state.
 """
 from __future__ import annotations
 
@@ -119,7 +120,6 @@ class ZeroStep:
         self._rows()
         self.hp = B.zero_adamw_hp(lr=adamw.lr, eps=adamw.eps, weight_decay=adamw.weight_decay)
         self.transient_hook = None  # called as hook(kind, unit, transient_rows) after each ZeRO-3 gather
-        self.timers = None          # micro_step: dict call name -> list of (start, end) CUDA events
         self.reset_state()
 
     def set_bucket_elems(self, bucket_elems: int) -> None:
@@ -148,19 +148,6 @@ class ZeroStep:
 
     def _s(self):
         return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
-
-    def _call(self, name: str, fn, *args):
-        """Issue one library call; with ``timers`` set, bracket it by CUDA
-        events recorded on the launching stream."""
-        if self.timers is None:
-            fn(*args)
-            return
-        s = self._s()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        fn(*args)
-        b.record(s)
-        self.timers.setdefault(name, []).append((a, b))
 
     # -- initialisation (plumbing, not part of the step) -------------------------
     def reset_state(self):
@@ -289,49 +276,17 @@ class ZeroStep:
     def micro_step(self, micro: int) -> None:
         """Process micro-batch ``micro`` (0-based) of ``n_micro``, whose 16-bit
         gradients are in ``grads``; the last one finishes the optimizer step.
-        ZeRO-1 accumulates locally in fp32 and reduce-scatters once (reading
-        notes §4.1); ZeRO-2 reduce-scatters every micro-batch into the fp32
-        shard (§4.2); ZeRO-3 also gathers every unit forward and backward for
-        every micro-batch (§4.3)."""
+        One zero_micro_step call: ZeRO-1 accumulates locally in fp32 and
+        reduce-scatters once (reading notes §4.1); ZeRO-2 reduce-scatters
+        every micro-batch into the fp32 shard (§4.2); ZeRO-3 also gathers
+        every unit forward and backward for every micro-batch (§4.3)."""
         M = self.n_micro
         if M == 1:
             self.step()
             return
         if not 0 <= micro < M:
             raise ValueError("micro out of range")
-        s = self._s()
-        L, C = self.L, self._call
-        last = micro == M - 1
-        if self.stage == 1:
-            C("accumulate", B.zero_accumulate_grads, L, micro, self.grad_rows, self.acc_rows, s)
-            if not last:
-                return
-            for b in reversed(range(self.n_buckets)):
-                C("reduce_scatter", B.zero_reduce_scatter_accumulated, L, b, self.acc_rows, self.gshard_rows, M,
-                  self.state, self.workspace, s)
-        elif self.stage == 2:
-            for b in reversed(range(self.n_buckets)):
-                C("reduce_scatter", B.zero_reduce_scatter_micro, L, b, micro, M, self.grad_rows, self.gshard_rows,
-                  self.state, self.workspace, s)
-            if not last:
-                return
-        else:
-            U = len(self.units)
-            for u in range(U):
-                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
-            for u in reversed(range(U)):
-                C("stage3_gather", B.zero_stage3_gather_layer, L, u, self.shard16_rows, self.transient_rows, s)
-                C("reduce_scatter", B.zero_reduce_scatter_micro, L, u, micro, M, self.grad_rows, self.gshard_rows,
-                  self.state, self.workspace, s)
-            if not last:
-                return
-        C("grad_norm", B.zero_grad_norm, L, self.max_norm, B.ZERO_NORM_DECIDE, self.state, self.workspace, s)
-        out = self.shard16_rows if (self.stage == 3 or not self.fuse_allgather) else self.param_rows
-        kind = B.ZERO_OUT_SHARDS if out is self.shard16_rows else B.ZERO_OUT_FULL_REPLICAS
-        C("adamw", B.zero_adamw_shard_step, L, self.hp, self.master_rows, self.m_rows, self.v_rows,
-          self.gshard_rows, self.state, out, kind, s)
-        if self.stage != 3 and not self.fuse_allgather:
-            C("allgather", B.zero_allgather_params, L, self.shard16_rows, self.param_rows, s)
+        B.zero_micro_step(self.L, self.step_args(), micro, M, self.acc_rows, self._s())
 
     # -- CUDA graph of one step -------------------------------------------------------
     def capture(self) -> torch.cuda.CUDAGraph:
