@@ -342,9 +342,12 @@ zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or_unit,
  * issued the gather of ZeRO-3 unit `unit` on `stream` (pass 0: forward, 1:
  * backward), before it issues anything else for that unit: the place where a
  * layer's forward or backward computation on the gathered unit would be
- * enqueued.  `transient` holds the N_d buffers that gather writes.  The hook
- * must not call zero_step or zero_step_from_host (the executor holds its
- * per-device lock). */
+ * enqueued.  `transient` holds the N_d buffers that gather writes.  With
+ * transient2, consecutive units' hooks get different streams: work that
+ * depends on the previous unit's (a layer's input is the previous layer's
+ * output) must be ordered by the caller, e.g. with an event.  The hook must
+ * not call zero_step, zero_micro_step or zero_step_from_host (the executor
+ * holds its per-device lock). */
 typedef void (*zero_unit_hook_fn)(void* user, int32_t pass, int32_t unit, void* const* transient,
                                   zero_stream_t stream);
 
