@@ -157,29 +157,27 @@ def make_layout(numels: Sequence[int], n_d: int, stage: int,
 
 def memory_formula_bytes(psi, n_d: int, stage: int, k: int = 12,
                          fp32_grad_accum: bool = False) -> Fraction:
-    """Per-GPU static model-state bytes.  16-bit params and grads (2 bytes
-    each), k bytes of optimizer state per parameter.
+    """Per-GPU static model-state bytes: the closed forms M0-M3 of "第 5 课：
+    ZeRO 与 FSDP" §2 (also the reading notes §4.1-§4.3: P_os, P_os+g,
+    P_os+g+p).  The three model-state terms are 16-bit parameters (2 Psi),
+    16-bit gradients (2 Psi) and k bytes of optimizer state per parameter;
+    stage s divides the last s of them by N_d:
       M0 = 2Psi + 2Psi + kPsi
       M1 = 2Psi + 2Psi + kPsi/N_d
       M2 = 2Psi + (2Psi + kPsi)/N_d
       M3 = (2Psi + 2Psi + kPsi)/N_d
-    FP32 gradient accumulation adds 4Psi for stages 0-1 and 4Psi/N_d for 2-3."""
+    FP32 gradient accumulation (the same section's note) adds a full-size fp32
+    buffer, 4Psi, while gradients are replicated (stages 0-1) and a 1/N_d
+    share of it once they are partitioned (stages 2-3)."""
     psi = Fraction(psi)
     if psi <= 0 or n_d <= 0 or stage not in (0, 1, 2, 3):
         raise ValueError("bad arguments")
-    p16, g16, opt = 2 * psi, 2 * psi, k * psi
-    extra = Fraction(0)
+    terms = (2 * psi, 2 * psi, k * psi)          # parameters, gradients, optimizer state
+    sharded = [i >= 3 - stage for i in range(3)]  # stage s partitions the last s terms
+    total = sum((t / n_d if sh else t) for t, sh in zip(terms, sharded))
     if fp32_grad_accum:
-        extra = 4 * psi if stage <= 1 else 4 * psi / n_d
-    if stage == 0:
-        base = p16 + g16 + opt
-    elif stage == 1:
-        base = p16 + g16 + opt / n_d
-    elif stage == 2:
-        base = p16 + (g16 + opt) / n_d
-    else:
-        base = (p16 + g16 + opt) / n_d
-    return base + extra
+        total += 4 * psi / n_d if sharded[1] else 4 * psi
+    return total
 
 
 def layout_memory_bytes(L: Layout) -> dict:
