@@ -649,3 +649,53 @@ def test_unit_hook_exceptions_reach_the_caller():
     eng.transient_hook = None
     eng.step()                                                            # the engine stays usable
     assert eng.read_state()["error"] == 0
+
+
+def test_two_host_threads_share_the_executor():
+    # two engines stepped from two host threads at once, each on its own stream: the executor's
+    # per-device lock serialises their issue; results equal the same engines stepped one by one
+    import threading
+    cases = [Case([120_000, 7, 50_001], 4, 2, FMT_BF16, bucket_elems=4096, per_tensor_scale=True),
+             Case(Z3_NUMELS, 2, 3, FMT_FP16, units=Z3_UNITS, max_norm=0.01, loss_scale=256.0, dynamic=True)]
+    kws = [{}, dict(live_units=2)]
+
+    def make():
+        out = []
+        for c, kw in zip(cases, kws):
+            L = c.layout()
+            e = _engine(c, **kw)
+            e.load_master(torch.from_numpy(c.master0(L)))
+            for r, g in enumerate(c.grads_torch(L, 1, c.loss_scale)):
+                e.grads[r].copy_(g.cuda())
+            out.append(e)
+        torch.cuda.synchronize()
+        return out
+
+    seq = make()
+    for e in seq:
+        for _ in range(5):
+            e.step()
+    torch.cuda.synchronize()
+    par = make()
+    errors = []
+
+    def worker(e):
+        try:
+            s = torch.cuda.Stream()
+            e.stream = s
+            for _ in range(5):
+                e.step()
+            s.synchronize()
+        except BaseException as ex:      # noqa: BLE001 (reported below)
+            errors.append(ex)
+
+    threads = [threading.Thread(target=worker, args=(e,)) for e in par]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for a, b in zip(seq, par):
+        for name in ("master", "m", "v", "state"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
