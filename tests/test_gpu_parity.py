@@ -699,3 +699,41 @@ def test_two_host_threads_share_the_executor():
     for a, b in zip(seq, par):
         for name in ("master", "m", "v", "state"):
             assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+@pytest.mark.parametrize("stage", [1, 2, 3])
+def test_fp16_subnormal_gradients(stage):
+    # fp16 gradients of std 2e-6 without loss scaling: most are fp16 subnormals (below 6.1e-5), so
+    # the reduce decodes them (and the cast writes subnormal parameters where the update makes them)
+    units = Z3_UNITS if stage == 3 else None
+    numels = Z3_NUMELS if stage == 3 else [120_000, 7, 50_001]
+    c = Case(numels, 4, stage, FMT_FP16, bucket_elems=32_768 if stage != 3 else 0, units=units, grad_std=2e-6,
+             max_norm=1e-4)
+    L = c.layout()
+    reps = c.grads(L, 1, 1.0)
+    h = np.concatenate(reps)
+    sub = ((h & 0x7C00) == 0) & ((h & 0x03FF) != 0)
+    assert sub.mean() > 0.5
+    run_parity(c, 3)
+
+
+def test_zero3_two_live_units_replay_from_a_graph():
+    # the executor's forks and joins between its streams capture into a CUDA graph; replays equal
+    # eager steps bit for bit
+    c = Case(Z3_NUMELS, 2, 3, FMT_BF16, units=Z3_UNITS, per_tensor_scale=True)
+    L = c.layout()
+    a, b = _engine(c, live_units=2), _engine(c, live_units=2)
+    for e in (a, b):
+        e.load_master(torch.from_numpy(c.master0(L)))
+        for r, g in enumerate(c.grads_torch(L, 1, 1.0)):
+            e.grads[r].copy_(g.cuda())
+    g = a.capture()
+    a.reset_state()
+    a.load_master(torch.from_numpy(c.master0(L)))
+    for _ in range(3):
+        g.replay()
+        b.step()
+    torch.cuda.synchronize()
+    for name in ("master", "m", "v", "shard16", "state"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert a.read_state()["t"] == 3
