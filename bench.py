@@ -749,7 +749,11 @@ def main():
             "config": workload_desc,
             "hbm_gbs": step_gbs, "hbm_pct_of_8tbs": 100.0 * step_gbs / NOMINAL_HBM_GBS,
             "hbm_frac_of_measured_copy": step_gbs / peak,
-            "gpu_launches": launches, "clocks": clk, "e2e": e2e, "roofline": roof, "cpu_baseline": cpu,
+            "gpu_launches": launches, "clocks": clk, "e2e": e2e, "roofline": roof,
+            # the whole step against the same peak: the step's algorithmic bytes over its time
+            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                              "frac": step_gbs / peak, "bytes_per_step": bpp * info.psi_pad},
+            "cpu_baseline": cpu,
             "kernels": kern, "graph": bool(args.graph),
             "last_step_state": {k: st[k] for k in ("t", "skipped", "overflow", "grad_norm", "clip_coef",
                                                    "loss_scale")}}
