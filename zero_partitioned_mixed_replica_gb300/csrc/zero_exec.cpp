@@ -1,6 +1,8 @@
 // Step executor: one whole ZeRO step as one library call, in the order the
-// pages give, from gradients resident in HBM (zero_step) or from gradient
-// replicas in host memory (zero_step_from_host).
+// pages give, from gradients resident in HBM (zero_step), from gradient
+// replicas in host memory (zero_step_from_host), or one micro-batch of an
+// accumulated step (zero_micro_step); plus the launch tracing of the calls it
+// issues.
 //
 // ZeRO-1/2: reduce-scatter bucket by bucket, last bucket first (backward
 // produces the last layers first: the mlqm.cn post "梯度桶化"; reading notes
