@@ -400,7 +400,7 @@ typedef struct zero_step_args {
  *     two buffer sets and between `stream` and one of the library's streams;
  *     every forward gather ends before the first update.
  * ZeRO-1/2 bucket launches of short buckets (mean at most 2^27 elements)
- * rotate over `stream` and three streams of the library's (created per device
+ * rotate over `stream` and seven streams of the library's (created per device
  * at the first call), which join `stream` again before the norm: consecutive
  * buckets touch disjoint elements and norm-partial slots, so one bucket's
  * launch can start while the previous one drains.  Results do not depend on

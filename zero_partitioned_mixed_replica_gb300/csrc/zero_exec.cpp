@@ -150,11 +150,13 @@ zero_status_t traced(int32_t kind, cudaStream_t st, Call&& call) {
 // lock per device serialises the calls that use them.
 // ---------------------------------------------------------------------------
 // Streams that short bucket launches rotate over (the caller's plus
-// kLanes - 1 of the library's).  GB300, GPT-2 small ZeRO-1, 25 buckets of
-// 5M elements, ms per step eager / from a CUDA graph: 2 lanes 1.081 / 1.074,
-// 3 lanes 1.065 / 1.052, 4 lanes 1.054 / 1.051.
+// kLanes - 1 of the library's).  GB300, ms per step eager / from a CUDA
+// graph.  GPT-2 small ZeRO-1, 25 buckets of 5M elements: 2 lanes 1.081 /
+// 1.074, 3 lanes 1.065 / 1.052, 4 lanes 1.054 / 1.051; 4, 6 and 8 lanes
+// equal on another box.  350M layout, N_d = 8, 3549 buckets of 1e5 elements:
+// 4 lanes 11.39 / 9.84, 6 lanes 8.39 / 7.06, 8 lanes 8.37 / 5.79.
 #ifndef ZK_BUCKET_LANES
-#define ZK_BUCKET_LANES 4
+#define ZK_BUCKET_LANES 8
 #endif
 constexpr int kLanes = ZK_BUCKET_LANES;
 static_assert(kLanes >= 2, "the executor needs a second stream");
