@@ -737,3 +737,18 @@ def test_zero3_two_live_units_replay_from_a_graph():
     for name in ("master", "m", "v", "shard16", "state"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
     assert a.read_state()["t"] == 3
+
+
+def test_long_run_with_natural_overflows():
+    # 200 steps, fp16 x a dynamic scale that doubles every 20 good steps from 2^16: once the scaled
+    # gradients pass 65504 they overflow on their own, the step is skipped and the scale halves, then
+    # grows again.  Flags, counters, scale, norm and state match the oracle at every step (beta^t
+    # after ~190 applied steps included); several buckets, rotating over the executor's streams.
+    c = Case([1000 * 512, 512, 487 * 1000, 2491], 4, 2, FMT_FP16, bucket_elems=4096 * 7 + 32, max_norm=1.0,
+             loss_scale=65536.0, dynamic=True, growth_interval=20, per_tensor_scale=True)
+    _, _, hist = run_parity(c, 200)
+    over = [g["overflow"] for g, _ in hist]
+    scales = [g["loss_scale"] for g, _ in hist]
+    assert sum(over) >= 2, over
+    assert max(scales) > 65536.0 and any(b < a for a, b in zip(scales, scales[1:]))
+    assert hist[-1][0]["t"] == 200 - sum(over)
