@@ -155,7 +155,8 @@ typedef struct zero_step_state {
 } zero_step_state;
 
 /* AdamW hyperparameters that may change between steps (lr schedules).  The
- * betas live in zero_step_state. */
+ * betas live in zero_step_state.  lr >= 0, weight_decay >= 0, eps > 0 also
+ * once rounded to binary32 (eps > 2^-150); anything else is ZERO_ERR_INVALID. */
 typedef struct zero_adamw_hp {
     double lr;
     double eps;

@@ -135,9 +135,10 @@ def test_step_calls_validate_before_launch():
     assert status(B.zero_adamw_shard_step, L3, hp, two, two, two, two, FAKE, two,
                   B.ZERO_OUT_FULL_REPLICAS, 0) == B.ZERO_ERR_STATE
     assert status(B.zero_adamw_shard_step, L, hp, two, two, two, two, FAKE, two, 9, 0) == B.ZERO_ERR_INVALID
-    bad_hp = B.zero_adamw_hp(lr=1e-3, eps=0.0, weight_decay=0.0)
-    assert status(B.zero_adamw_shard_step, L, bad_hp, two, two, two, two, FAKE, two,
-                  B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_INVALID
+    for eps in (0.0, 2.0 ** -150, -1e-8, float("nan")):   # 2^-150 rounds to a binary32 zero
+        bad_hp = B.zero_adamw_hp(lr=1e-3, eps=eps, weight_decay=0.0)
+        assert status(B.zero_adamw_shard_step, L, bad_hp, two, two, two, two, FAKE, two,
+                      B.ZERO_OUT_SHARDS, 0) == B.ZERO_ERR_INVALID, eps
     assert status(B.zero_allgather_params, L3, two, two, 0) == B.ZERO_ERR_STATE
     assert status(B.zero_stage3_gather_layer, L, 0, two, two, 0) == B.ZERO_ERR_STATE
     assert status(B.zero_stage3_gather_layer, L3, 2, two, two, 0) == B.ZERO_ERR_INVALID

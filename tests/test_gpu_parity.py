@@ -10,6 +10,7 @@ the binary32 partials).  Bitwise equality of the state is
 also asserted wherever GPU and oracle used the same clip coefficient (always,
 when the oracle is re-run with the GPU's coefficient)."""
 import math
+from dataclasses import dataclass
 
 import numpy as np
 import pytest
@@ -332,6 +333,57 @@ def test_zero_gradients_apply_weight_decay_only():
     eng, zs, _ = run_parity(c, 2)
     assert float(eng.read_state()["grad_norm"]) == 0.0
     assert not eng.m.any() and not eng.v.any()
+
+
+@dataclass
+class _ZeroRegions(Case):
+    """Tensors in `zero_tensors` get zero gradients of both signs on every rank
+    at every step, so their g, m and v stay zero: the update kernels' short path
+    for all-zero elements (and, where a 4- or 8-element group straddles a
+    tensor edge, the plain update on a mixed group).  Half of their master
+    weights start at +0 or -0, so the zero signs of p1 - step_size * m matter."""
+    zero_tensors: tuple = ()
+
+    def master0(self, L):
+        m = super().master0(L).copy()
+        for t in self.zero_tensors:
+            o, n = L.tensor_offsets[t], L.numels[t]
+            m[o:o + n // 4] = 0.0
+            m[o + n // 4:o + n // 2] = -0.0
+        return m
+
+    def grads_torch(self, L, step, loss_scale, device="cpu"):
+        out = super().grads_torch(L, step, loss_scale, device)
+        for r, g in enumerate(out):
+            for t in self.zero_tensors:
+                o, n = L.tensor_offsets[t], L.numels[t]
+                bits = torch.zeros(n, dtype=torch.int16)
+                bits[(torch.arange(n) + r + step) % 3 == 0] = -0x8000      # -0 in fp16 and bf16
+                g.view(torch.int16)[o:o + n] = bits
+        return out
+
+
+@pytest.mark.parametrize("n_d,stage,max_norm,fmt", [
+    (4, 2, 1.0, FMT_FP16),    # split step: the TMA update
+    (4, 1, 1.0, FMT_BF16),    # split step: the TMA update
+    (2, 2, 1.0, FMT_BF16),    # N_d = 2: the LDG update
+    (4, 3, 1.0, FMT_FP16),    # 16-bit shards: the LDG update
+    (4, 2, 0.0, FMT_FP16),    # fused per-bucket update
+    (3, 3, 0.0, FMT_BF16),    # fused update into 16-bit shards
+])
+def test_zero_state_regions_in_every_update_kernel(n_d, stage, max_norm, fmt):
+    # a 300k-element zero tensor spans ~150 TMA tiles; the 33- and 5-element ones sit between dense
+    # tensors, so groups straddle zero and non-zero elements
+    c = _ZeroRegions([70_001, 300_000, 33, 90_000, 5, 40_000], n_d, stage, fmt, bucket_elems=65_536,
+                     max_norm=max_norm, loss_scale=1024.0 if fmt == FMT_FP16 else 1.0,
+                     units=[0, 0, 1, 1, 2, 2] if stage == 3 else None, zero_tensors=(1, 2, 4))
+    eng, zs, _ = run_parity(c, 3)
+    L = c.layout()
+    for name in ("m", "v"):
+        flat = zs.flat(name)
+        for t in c.zero_tensors:
+            o = L.tensor_offsets[t]
+            assert not flat[o:o + L.numels[t]].any(), (name, t)   # the case does exercise zero state
 
 
 def test_units_smaller_than_a_rank_slice():

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads) rs_acc_kernel(const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 bad |= !isfinite(s[e]);
-                g[e] = __fdiv_rn(s[e], D);
+                g[e] = div_rn(s[e], D);
             }
             const uint32_t k = v - a.seg.seg_v;
             const uint32_t r = k / a.seg.shard_v;

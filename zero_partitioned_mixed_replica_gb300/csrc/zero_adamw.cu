@@ -63,17 +63,25 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     const uint64_t S = (uint64_t)a.shard_v * kVec;
     const uint32_t ntile = (uint32_t)((S + TE - 1) / TE);
     const uint32_t total = ntile * (uint32_t)nd;
-    // Each CTA takes a contiguous range of tiles.  GB300, 1.5B launch: 10.68 ms
-    // against 10.73 ms with tiles dealt round-robin over the CTAs; rotating the
-    // order of the replica stores per CTA instead cost 13% (12.14 ms): the CTAs
-    // writing the same replica region at about the same time is what DRAM
-    // rewards.
-    const uint32_t chunk = (total + gridDim.x - 1) / gridDim.x;
-    const uint32_t first = blockIdx.x * chunk, stride = 1u;
-    const uint32_t count = first < total ? min(chunk, total - first) : 0u;
+    // Tiles are dealt to the CTAs in batches of kBatch consecutive tiles,
+    // round-robin: CTA c takes batches c, c + G, c + 2G, ...  An element whose
+    // gradient and moments are all zero (an embedding row no batch has touched
+    // yet) sends both divisions of the update down their slow path and costs
+    // about twice a dense one; dealt this way a contiguous zero region spreads
+    // over every CTA.  GB300, 1.5B launch, dense / word-embedding gradients
+    // zero: 10.71 / 11.25 ms; one contiguous range per CTA: 10.68 / 20.91 ms
+    // (the few CTAs holding the zero region set the time); single tiles
+    // round-robin: 10.73 / 11.27; batches of 16 or 64: 10.77 or 10.87 ms
+    // dense (a batch-sized tail).
+    constexpr uint32_t kBatch = 4;
+    const uint32_t nbatch = (total + kBatch - 1) / kBatch;
+    const uint32_t G = gridDim.x, c = blockIdx.x;
+    const uint32_t mine = c < nbatch ? (nbatch - c + G - 1) / G : 0u;
+    const bool has_last = mine > 0 && c + (mine - 1) * G == nbatch - 1;  // the short batch is a CTA's last
+    const uint32_t count = mine * kBatch - (has_last ? nbatch * kBatch - total : 0u);
 
     auto tile_of = [&](uint32_t kk, uint32_t& r, uint64_t& j0, uint32_t& len) {
-        const uint32_t T = first + kk * stride;
+        const uint32_t T = (c + (kk / kBatch) * G) * kBatch + kk % kBatch;
         r = T / ntile;
         j0 = (uint64_t)(T - r * ntile) * TE;
         const uint64_t rem = S - j0;
@@ -123,6 +131,9 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
                     float4 p4 = *reinterpret_cast<const float4*>(src + TE + e);
                     float4 m4 = *reinterpret_cast<const float4*>(src + 2 * TE + e);
                     float4 v4 = *reinterpret_cast<const float4*>(src + 3 * TE + e);
+                    // the plain update: a zero-state test here (as in the other update
+                    // kernels) evens out zero regions but cost 4% on dense gradients
+                    // (1.5B launch 11.12 against 10.68 ms)
                     adamw1(p4.x, m4.x, v4.x, g4.x, k);
                     adamw1(p4.y, m4.y, v4.y, g4.y, k);
                     adamw1(p4.z, m4.z, v4.z, g4.z, k);
@@ -205,8 +216,13 @@ __global__ void __launch_bounds__(kThreads, 4) adamw_ldg_kernel(const __grid_con
         ld8(a.master[r] + o, p);
         ld8(a.m[r] + o, m);
         ld8(a.v[r] + o, w);
+        if (all_zero8x3(g, m, w)) {  // e.g. padding, untouched embedding rows
 #pragma unroll
-        for (int e = 0; e < 8; ++e) adamw1(p[e], m[e], w[e], g[e], k);
+            for (int e = 0; e < 8; ++e) adamw1_zero_state(p[e], m[e], w[e], g[e], k);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) adamw1(p[e], m[e], w[e], g[e], k);
+        }
         st8(a.master[r] + o, p);
         st8(a.m[r] + o, m);
         st8(a.v[r] + o, w);
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constan
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 bad |= !isfinite(s[e]);
-                g[e] = __fdiv_rn(s[e], D);
+                g[e] = div_rn(s[e], D);
             }
             const uint32_t kk = v - a.seg.seg_v;
             const uint32_t r = kk / a.seg.shard_v;
@@ -261,8 +277,13 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constan
             ld8(a.master[r] + o, p);
             ld8(a.m[r] + o, m);
             ld8(a.v[r] + o, w);
+            if (all_zero8x3(g, m, w)) {  // e.g. padding, untouched embedding rows
 #pragma unroll
-            for (int e = 0; e < 8; ++e) adamw1(p[e], m[e], w[e], g[e], k);
+                for (int e = 0; e < 8; ++e) adamw1_zero_state(p[e], m[e], w[e], g[e], k);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) adamw1(p[e], m[e], w[e], g[e], k);
+            }
             st8(a.master[r] + o, p);
             st8(a.m[r] + o, m);
             st8(a.v[r] + o, w);
@@ -389,8 +410,11 @@ static zero_status_t launch_fused(const zk::FusedArgs& a, int64_t nvec, int out_
 
 static zero_status_t check_hp(const zero_adamw_hp* hp, const char* what) {
     if (!hp) return fail(ZERO_ERR_INVALID, std::string(what) + ": NULL hyperparameters");
-    if (!(hp->lr >= 0.0) || !(hp->eps > 0.0) || !(hp->weight_decay >= 0.0))
-        return fail(ZERO_ERR_INVALID, std::string(what) + ": need lr >= 0, eps > 0, weight_decay >= 0");
+    // eps must stay positive in binary32 too: the update divides by a den of at
+    // least eps, and the short path for all-zero elements relies on den > 0
+    if (!(hp->lr >= 0.0) || !(hp->eps > 0.0) || !((float)hp->eps > 0.0f) || !(hp->weight_decay >= 0.0))
+        return fail(ZERO_ERR_INVALID, std::string(what) +
+                                          ": need lr >= 0, eps > 0 (also as a binary32), weight_decay >= 0");
     return ZERO_OK;
 }
 

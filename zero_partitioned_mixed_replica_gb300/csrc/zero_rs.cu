@@ -26,7 +26,7 @@ __device__ __forceinline__ void rs_combine(float (&s)[8], const float* accp, flo
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             bad |= !isfinite(s[e]);
-            s[e] = __fdiv_rn(s[e], D);
+            s[e] = div_rn(s[e], D);
         }
     } else if constexpr (MODE == RS_FIRST) {
         (void)accp;
@@ -38,7 +38,7 @@ __device__ __forceinline__ void rs_combine(float (&s)[8], const float* accp, flo
             const float t = __fadd_rn(acc[e], s[e]);
             if constexpr (MODE == RS_LAST) {
                 bad |= !isfinite(t);
-                s[e] = __fdiv_rn(t, D);
+                s[e] = div_rn(t, D);
             } else {
                 s[e] = t;
             }
