@@ -464,8 +464,9 @@ def gpu_run(args, w, rank, world, local_rank):
             def e2e_step():
                 if args.micro == 1:
                     # one C-ABI call (zero_step_from_host): the per-bucket host-to-device copies
-                    # overlap the reduce-scatter, and the step state is copied back to host_state
-                    eng.step_from_host(host_grads, state_out=host_state)
+                    # overlap the reduce-scatter and, from the second step on, the previous step's
+                    # norm and update; the step state is copied back to host_state
+                    eng.step_from_host(host_grads, state_out=host_state, overlap_previous=True)
                 else:
                     for mb in range(args.micro):
                         eng.upload_grads(host_grads)
@@ -501,6 +502,7 @@ def gpu_run(args, w, rank, world, local_rank):
                    "h2d_bytes_per_step": int(eng.grads.numel() * eng.grads.element_size()) * args.micro,
                    "d2h_bytes_per_step": 96, "ms_per_step": ems / args.e2e_steps,
                    "warmup_steps": max(3, args.warmup), "host_link_gbs": link_gbs,
+                   "overlap_previous": args.micro == 1,
                    "h2d_floor_ms": int(eng.grads.numel() * eng.grads.element_size()) * args.micro / link_gbs / 1e6,
                    "copy_only_ms": min(copy_ms),
                    "ms_each": [round(evs[i].elapsed_time(evs[i + 1]), 2) for i in range(args.e2e_steps)]}

@@ -208,6 +208,9 @@ def test_executor_and_cast_validate_before_launch():
     assert status(B.zero_step_from_host, L, args(L, False), [FAKE, 0], 0, None, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_step_from_host, L, args(L, True, max_norm=0.5), two, 0, None, 0) == B.ZERO_ERR_INVALID
     assert status(B.zero_step_from_host, L, args(L, False, full=[FAKE, MIS]), two, 0, None, 0) == B.ZERO_ERR_ALIGN
+    bad_flag = args(L, False)
+    bad_flag.args.overlap_previous = 2
+    assert status(B.zero_step, L, bad_flag, 0) == B.ZERO_ERR_INVALID                  # the flag is 0 or 1
     assert B.lib().zero_trace_read(None, 0) == B.ZERO_ERR_INVALID
     assert B.zero_trace_read() == {}             # nothing traced: no kind reported
     L1 = B.zero_layout_init([1000, 24], None, 2, 1, 0, 0, B.ZERO_BF16)

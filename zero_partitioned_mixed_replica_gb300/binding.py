@@ -101,7 +101,7 @@ class zero_step_args(ctypes.Structure):
                  "transient")] + \
                [("state", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("transient2", ctypes.POINTER(ctypes.c_void_p)), ("unit_hook", ZERO_UNIT_HOOK),
-                ("hook_user", ctypes.c_void_p)]
+                ("hook_user", ctypes.c_void_p), ("overlap_previous", ctypes.c_int32)]
 
 
 class StepArgs:
@@ -400,9 +400,11 @@ def zero_micro_step(L: Layout, args: StepArgs, micro: int, n_micro: int, acc_rep
 
 
 def zero_step_from_host(L: Layout, args: StepArgs, host_grads, chunk_elems: int = 0, host_state=None,
-                        stream=None) -> None:
+                        stream=None, overlap_previous: bool = False) -> None:
     """host_grads: one host pointer (or CPU tensor) per rank; host_state: a
-    CPU tensor / address of 96 bytes, or None."""
+    CPU tensor / address of 96 bytes, or None; overlap_previous sets the
+    field of the same name in ``args`` for this call."""
+    args.args.overlap_previous = int(bool(overlap_previous))
     args.hook_error = None
     status = lib().zero_step_from_host(L, ctypes.byref(args.args), _ptrs(host_grads, L), int(chunk_elems),
                                        _addr(host_state), _stream(stream))

@@ -58,6 +58,8 @@ zero_status_t check_args(const zero_layout* L, const zero_step_args* a, const ch
     if (!a) return fail(ZERO_ERR_INVALID, w + ": NULL arguments");
     if (L->stage == 0) return fail(ZERO_ERR_STATE, w + ": stage 0 has no partitioned step");
     if (a->fused != 0 && a->fused != 1) return fail(ZERO_ERR_INVALID, w + ": fused must be 0 or 1");
+    if (a->overlap_previous != 0 && a->overlap_previous != 1)
+        return fail(ZERO_ERR_INVALID, w + ": overlap_previous must be 0 or 1");
     if (a->fused && a->max_norm > 0.0)
         return fail(ZERO_ERR_INVALID, w + ": the fused step cannot clip (use fused = 0)");
     if (!a->fused && !a->grad_shards) return fail(ZERO_ERR_INVALID, w + ": the split step needs grad_shards");
@@ -168,6 +170,11 @@ struct DeviceRes {
     cudaStream_t cs[2] = {nullptr, nullptr};
     cudaEvent_t start = nullptr;
     std::vector<cudaEvent_t> ev;  // two per bucket: one per copy stream
+    // Recorded by zero_step_from_host after its last launch that reads the
+    // device replicas; released_ok says that call succeeded outside a capture
+    // and no other executor call has run on the device since.
+    cudaEvent_t released = nullptr;
+    bool released_ok = false;
 };
 DeviceRes g_res[64];
 
@@ -270,9 +277,16 @@ struct Micro {
     bool last() const { return micro == n_micro - 1; }
 };
 
+// `released`, if not null, is recorded on `s` once every launch that reads
+// the gradient replicas has been issued (and joined to `s`).
 zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream_t s, DeviceRes& R,
-                       const Ready& ready, const Micro& mb = Micro()) {
+                       const Ready& ready, const Micro& mb = Micro(), cudaEvent_t released = nullptr) {
     zero_status_t rc;
+    auto release = [&]() -> zero_status_t {
+        if (!released) return ZERO_OK;
+        cudaError_t e = cudaEventRecord(released, s);
+        return e == cudaSuccess ? ZERO_OK : cuda_fail("zero_step: record", e);
+    };
     const int32_t nb = (int32_t)L->buckets.size();
     const zero_stream_t zs = reinterpret_cast<zero_stream_t>(s);
     // the reduction of bucket (ZeRO-3: unit) k on stream `st`
@@ -338,6 +352,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             if ((rc = reduce(u, zst, a->param16_shards, ZERO_OUT_SHARDS)) != ZERO_OK) return rc;
         }
         if ((rc = fork.join()) != ZERO_OK) return rc;
+        if ((rc = release()) != ZERO_OK) return rc;
         if (!mb.last()) return ZERO_OK;  // more micro-batches to reduce before the update
         if (a->fused)
             return traced(ZERO_CALL_GRAD_NORM, s, [&] {
@@ -370,6 +385,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
                                         a->param16_full, ZERO_OUT_FULL_REPLICAS, a->workspace, zs);
              })) != ZERO_OK)
             return rc;
+        if ((rc = release()) != ZERO_OK) return rc;
     } else {
         // rotate only short buckets: a launch's ramp and drain cost a few
         // microseconds, which matters at 5M-50M elements per bucket, not at 500M
@@ -384,6 +400,7 @@ zero_status_t run_step(const zero_layout* L, const zero_step_args* a, cudaStream
             if ((rc = reduce(b, zb, a->param16_full, ZERO_OUT_FULL_REPLICAS)) != ZERO_OK) return rc;
         }
         if ((rc = fork.join()) != ZERO_OK) return rc;
+        if ((rc = release()) != ZERO_OK) return rc;
         if (!mb.last()) return ZERO_OK;  // ZeRO-2: more micro-batches before the update
     }
     if (a->fused)
@@ -418,6 +435,7 @@ extern "C" zero_status_t zero_step(const zero_layout* L, const zero_step_args* a
     DeviceRes* R = nullptr;
     if ((rc = current_res(&R, "zero_step")) != ZERO_OK) return rc;
     std::lock_guard<std::mutex> lock(R->mu);  // the fork/join events are shared by the device's calls
+    R->released_ok = false;                    // this step reads the replicas on `stream`
     if ((rc = step_res(*R, "zero_step")) != ZERO_OK) return rc;
     return run_step(L, a, reinterpret_cast<cudaStream_t>(stream), *R,
                     [](int32_t, cudaStream_t) { return ZERO_OK; });
@@ -441,6 +459,7 @@ extern "C" zero_status_t zero_micro_step(const zero_layout* L, const zero_step_a
     DeviceRes* R = nullptr;
     if ((rc = current_res(&R, what)) != ZERO_OK) return rc;
     std::lock_guard<std::mutex> lock(R->mu);
+    R->released_ok = false;
     if ((rc = step_res(*R, what)) != ZERO_OK) return rc;
     Micro mb;
     mb.micro = micro;
@@ -467,10 +486,13 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
     DeviceRes* R = nullptr;
     if ((rc = current_res(&R, what)) != ZERO_OK) return rc;
     std::lock_guard<std::mutex> lock(R->mu);  // the events are reused by every call on this device
+    const bool prev_released = R->released_ok;
+    R->released_ok = false;
     if ((rc = step_res(*R, what)) != ZERO_OK) return rc;
     for (int i = 0; i < 2; ++i)
         if ((rc = make_stream(&R->cs[i], what)) != ZERO_OK) return rc;
     if ((rc = make_event(&R->start, what)) != ZERO_OK) return rc;
+    if ((rc = make_event(&R->released, what)) != ZERO_OK) return rc;
     const int32_t nb = (int32_t)L->buckets.size();
     while (R->ev.size() < 2 * (size_t)nb) {
         cudaEvent_t x = nullptr;
@@ -479,10 +501,19 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
     }
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    // the previous step on `stream` has finished reading the replicas before they are overwritten
-    if ((e = cudaEventRecord(R->start, s)) != cudaSuccess) return cuda_fail("zero_step_from_host: record", e);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail("zero_step_from_host: capture query", e);
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    // The previous step has finished reading the replicas before they are
+    // overwritten: all work queued on `stream`, or, with overlap_previous,
+    // the previous call's last replica-reading launch (and what came before).
+    cudaEvent_t gate = R->released;
+    if (!(a->overlap_previous && prev_released && !capturing)) {
+        if ((e = cudaEventRecord(R->start, s)) != cudaSuccess) return cuda_fail("zero_step_from_host: record", e);
+        gate = R->start;
+    }
     for (int i = 0; i < 2; ++i)
-        if ((e = cudaStreamWaitEvent(R->cs[i], R->start, 0)) != cudaSuccess)
+        if ((e = cudaStreamWaitEvent(R->cs[i], gate, 0)) != cudaSuccess)
             return cuda_fail("zero_step_from_host: wait", e);
     // copies in the order the step consumes the buckets (units): last first
     const size_t esz = sizeof(uint16_t);
@@ -502,18 +533,22 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
             if ((e = cudaEventRecord(R->ev[2 * k + q], R->cs[q])) != cudaSuccess)
                 return cuda_fail("zero_step_from_host: record", e);
     }
-    rc = run_step(L, a, s, *R, [&](int32_t k, cudaStream_t on) -> zero_status_t {
-        for (int q = 0; q < 2; ++q) {
-            cudaError_t w = cudaStreamWaitEvent(on, R->ev[2 * k + q], 0);
-            if (w != cudaSuccess) return cuda_fail("zero_step_from_host: wait", w);
-        }
-        return ZERO_OK;
-    });
+    rc = run_step(
+        L, a, s, *R,
+        [&](int32_t k, cudaStream_t on) -> zero_status_t {
+            for (int q = 0; q < 2; ++q) {
+                cudaError_t w = cudaStreamWaitEvent(on, R->ev[2 * k + q], 0);
+                if (w != cudaSuccess) return cuda_fail("zero_step_from_host: wait", w);
+            }
+            return ZERO_OK;
+        },
+        Micro(), capturing ? nullptr : R->released);
     if (rc != ZERO_OK) return rc;
     if (host_state) {
         e = cudaMemcpyAsync(host_state, a->state, sizeof(zero_step_state), cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail("zero_step_from_host: state read-back", e);
     }
+    R->released_ok = !capturing;
     return ZERO_OK;
 }
 

@@ -316,7 +316,7 @@ class ZeroStep:
             raise ValueError("overlapped host copies need pinned host memory")
 
     def step_from_host(self, host: torch.Tensor, chunk_elems: int = 1 << 27,
-                       state_out: Optional[torch.Tensor] = None) -> None:
+                       state_out: Optional[torch.Tensor] = None, overlap_previous: bool = False) -> None:
         """One step whose N_d gradient replicas come from pinned host memory,
         through the library's zero_step_from_host: each bucket's range
         (ZeRO-3: each unit's) is copied on the library's two copy streams in
@@ -328,19 +328,29 @@ class ZeroStep:
         stands in for backward).  ``state_out`` (96 bytes of host memory,
         pinned for an asynchronous copy) receives the step state at the end
         of the step.  The result is identical to ``upload_grads(host)`` then
-        ``step()``."""
+        ``step()``.
+
+        ``overlap_previous``: when the previous library step of this device
+        was also a host-input step, this step's copies start as soon as that
+        step has reduced its replicas, so its norm and update overlap them.
+        The device replicas (``grads``) must then not be touched in between;
+        ``upload_grads`` since the last host-input step turns the overlap off
+        for the next one."""
         self._check_host(host, True)
         if state_out is not None and (state_out.device.type != "cpu" or state_out.numel() * state_out.element_size()
                                       < self.state.numel()):
             raise ValueError("state_out must be a host tensor of at least 96 bytes")
+        overlap = overlap_previous and not getattr(self, "_grads_written", False)
+        self._grads_written = False
         B.zero_step_from_host(self.L, self.step_args(), [host[r] for r in range(self.n_d)], chunk_elems,
-                              state_out, self._s())
+                              state_out, self._s(), overlap_previous=overlap)
 
     def upload_grads(self, host: torch.Tensor, chunk_elems: int = 1 << 27) -> None:
         """Copy the N_d gradient replicas from (pinned) host memory, in chunks
         alternating over two copy streams (faster than one large copy on this
         part), ordered before the next library call on the step's stream."""
         self._check_host(host, False)
+        self._grads_written = True
         if getattr(self, "_copy_streams", None) is None:
             self._copy_streams = [torch.cuda.Stream(self.device) for _ in range(2)]
         cur = self._s()
