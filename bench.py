@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="gpt2_xl")
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-blocks", type=int, default=0,
                    help="oracle timing on the workload's first N transformer blocks (0: the cpu_baseline "
                         "takes about 10-30 s of blocks; the reference arm takes the whole layout if it fits)")
@@ -473,11 +473,6 @@ def gpu_run(args, w, rank, world, local_rank):
                         eng.micro_step(mb)
                     host_state.copy_(eng.state, non_blocking=True)
 
-            # Untimed warm-up, as for the device-resident steps: the first
-            # whole-buffer passes over a freshly pinned buffer cross the host
-            # link at 90-140 GB/s before settling at the link rate.
-            for _ in range(max(3, args.warmup)):
-                e2e_step()
             # the copies alone (same chunks on the same two streams), to read the e2e value against
             copy_ms = []
             for _ in range(2):
@@ -487,6 +482,12 @@ def gpu_run(args, w, rank, world, local_rank):
                 c1.record(stream)
                 c1.synchronize()
                 copy_ms.append(c0.elapsed_time(c1))
+            # Untimed warm-up, as for the device-resident steps: the first
+            # whole-buffer passes over a freshly pinned buffer cross the host
+            # link at 90-140 GB/s before settling at the link rate.  After it,
+            # every step's copies overlap the previous step's update.
+            for _ in range(max(3, args.warmup)):
+                e2e_step()
             torch.cuda.synchronize(dev)
             if world > 1:
                 dist.barrier()
