@@ -5,8 +5,9 @@ elements, bucket sizes from 32 elements to the whole buffer, bf16 and fp16
 an overflow planted in one rank at step 2 on the split path, the fused and
 split paths, per-bucket and whole-buffer fused launches, an unfused
 all-gather, random ZeRO-3 unit groupings with one or two live units, and
-larger pad multiples.  Each case's parameters come from its seed alone, and
-the case id names them."""
+larger pad multiples; a third of the cases again with the replicas in pinned
+host memory (zero_step_from_host, chunks of random size).  Each case's
+parameters come from its seed alone, and the case id names them."""
 import numpy as np
 import pytest
 import torch
@@ -79,5 +80,16 @@ def _id(seed: int) -> str:
 def test_random_layout_matches_the_oracle(seed):
     c, kw = draw_case(seed)
     _, _, hist = run_parity(c, 3, use_gpu_clip=True, **kw)
+    if c.inf_step is not None:
+        assert [g["overflow"] for g, _ in hist] == [0, 1, 0]
+
+
+@pytest.mark.parametrize("seed", range(0, N_CASES, 3), ids=[_id(s) for s in range(0, N_CASES, 3)])
+def test_random_layout_from_host_memory_matches_the_oracle(seed):
+    # the same layouts with the replicas coming from pinned host memory through
+    # zero_step_from_host, in chunks of a random size (a multiple of 8 elements)
+    c, kw = draw_case(seed)
+    chunk = 8 * int(np.random.default_rng(seed).integers(1, 40_000))
+    _, _, hist = run_parity(c, 3, use_gpu_clip=True, host_input=chunk, **kw)
     if c.inf_step is not None:
         assert [g["overflow"] for g, _ in hist] == [0, 1, 0]
