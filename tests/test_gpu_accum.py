@@ -30,7 +30,7 @@ def _run(c: Case, M: int, steps: int, use_gpu_clip: bool = False, live_units: in
     L = c.layout()
     eng = ZeroStep(c.numels, c.n_d, c.stage, c.fmt, c.bucket_elems, c.units,
                    AdamW(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay), c.max_norm, c.loss_scale,
-                   c.dynamic, c.growth_interval, n_micro=M, live_units=live_units)
+                   c.dynamic, c.growth_interval, n_micro=M, live_units=live_units, pad_multiple=c.pad_multiple)
     m0 = c.master0(L)
     eng.load_master(torch.from_numpy(m0))
     zs = ZeroSimulation(L, m0, c.fmt, HP, max_norm=c.max_norm, loss_scale=c.loss_scale, dynamic=c.dynamic,

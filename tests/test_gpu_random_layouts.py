@@ -6,7 +6,8 @@ an overflow planted in one rank at step 2 on the split path, the fused and
 split paths, per-bucket and whole-buffer fused launches, an unfused
 all-gather, random ZeRO-3 unit groupings with one or two live units, and
 larger pad multiples; a third of the cases again with the replicas in pinned
-host memory (zero_step_from_host, chunks of random size).  Each case's
+host memory (zero_step_from_host, chunks of random size), and another third
+accumulated over 2-4 micro-batches (zero_micro_step).  Each case's
 parameters come from its seed alone, and the case id names them."""
 import numpy as np
 import pytest
@@ -93,3 +94,13 @@ def test_random_layout_from_host_memory_matches_the_oracle(seed):
     _, _, hist = run_parity(c, 3, use_gpu_clip=True, host_input=chunk, **kw)
     if c.inf_step is not None:
         assert [g["overflow"] for g, _ in hist] == [0, 1, 0]
+
+
+@pytest.mark.parametrize("seed", range(1, N_CASES, 3), ids=[_id(s) for s in range(1, N_CASES, 3)])
+def test_random_layout_with_gradient_accumulation_matches_the_oracle(seed):
+    # the same layouts accumulated over 2-4 micro-batches (zero_micro_step; the split step),
+    # against the oracle's accumulation order for the stage
+    from tests.test_gpu_accum import _run
+    c, kw = draw_case(seed)
+    M = int(np.random.default_rng(seed).integers(2, 5))
+    _run(c, M=M, steps=2, use_gpu_clip=True, live_units=kw.get("live_units", 1))
