@@ -428,14 +428,16 @@ zero_status_t zero_step(const zero_layout* L, const zero_step_args* args, zero_s
  * reduced as soon as it is filled).  The copies start after the work already
  * queued on `stream` (the previous step reads the same device replicas),
  * except with args->overlap_previous = 1: when the previous executor call on
- * this device was a zero_step_from_host call that succeeded outside a graph
+ * this device was a zero_step_from_host call on the same `stream` with the
+ * same device replicas (args->grad_replicas) that succeeded outside a graph
  * capture, the copies then wait only for that call's last launch that reads
  * the device replicas (its reduce-scatters or fused updates, and everything
  * queued before them), so its norm and update overlap this step's copies.
  * The caller must then queue nothing between the two calls that reads or
  * writes the device replicas: they are the library's staging buffers.  Any
- * zero_step or zero_micro_step call in between, a capturing `stream`, or a
- * failed previous call makes the copies wait for all work queued on `stream`.
+ * zero_step or zero_micro_step call in between, another stream or other
+ * device replicas than the previous call's, a capturing `stream`, or a failed
+ * previous call makes the copies wait for all work queued on `stream`.
  * host_state: host pointer to sizeof(zero_step_state) bytes, or NULL; the
  * step state is copied there at the end of the step, on `stream`.
  * Asynchronous: synchronise `stream` before reading host_state or reusing

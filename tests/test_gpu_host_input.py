@@ -186,3 +186,35 @@ def test_other_steps_between_host_steps_turn_the_overlap_off():
     for s in range(5):
         _oracle_step(zs, reps[s], outs[s])
     _compare_final(c, eng, zs)
+
+
+def test_two_engines_on_two_streams_alternate_overlapped_host_steps():
+    # engines A and B (own buffers, own streams) alternate host-input steps with overlap_previous,
+    # queued without synchronisation: each call's previous executor call is the other engine's,
+    # on another stream with other device replicas, so each must wait for its own stream instead
+    # of the other engine's release; both match their oracles bit for bit
+    from zero_partitioned_mixed_replica_gb300.engine import AdamW, ZeroStep
+    cases = [_queued_case(2, False), _queued_case(2, False)]
+    cases[1].seed = 4321
+    engs, sims, data = [], [], []
+    for c in cases:
+        L = c.layout()
+        eng = ZeroStep(c.numels, c.n_d, c.stage, c.fmt, c.bucket_elems, c.units,
+                       AdamW(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay), c.max_norm, c.loss_scale,
+                       c.dynamic, c.growth_interval, stream=torch.cuda.Stream())
+        m0 = c.master0(L)
+        eng.load_master(torch.from_numpy(m0))
+        engs.append(eng)
+        sims.append(ZeroSimulation(L, m0, c.fmt, HP, max_norm=c.max_norm, loss_scale=c.loss_scale))
+        data.append(_pinned_steps(c, L, eng, 3))
+    torch.cuda.synchronize()
+    for s in range(3):
+        for k in (0, 1):
+            hosts, _, outs = data[k]
+            engs[k].step_from_host(hosts[s], chunk_elems=30_000, state_out=outs[s], overlap_previous=True)
+    torch.cuda.synchronize()
+    for k in (0, 1):
+        _, reps, outs = data[k]
+        for s in range(3):
+            _oracle_step(sims[k], reps[s], outs[s])
+        _compare_final(cases[k], engs[k], sims[k])

@@ -172,9 +172,14 @@ struct DeviceRes {
     std::vector<cudaEvent_t> ev;  // two per bucket: one per copy stream
     // Recorded by zero_step_from_host after its last launch that reads the
     // device replicas; released_ok says that call succeeded outside a capture
-    // and no other executor call has run on the device since.
+    // and no other executor call has run on the device since.  The call's
+    // stream and device replica pointers: a later call takes the early gate
+    // only with the same ones (another set of replicas was last read by a
+    // step this event does not follow).
     cudaEvent_t released = nullptr;
     bool released_ok = false;
+    cudaStream_t released_stream = nullptr;
+    std::vector<const void*> released_grads;
 };
 DeviceRes g_res[64];
 
@@ -507,8 +512,10 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
     // The previous step has finished reading the replicas before they are
     // overwritten: all work queued on `stream`, or, with overlap_previous,
     // the previous call's last replica-reading launch (and what came before).
+    bool same = prev_released && R->released_stream == s && R->released_grads.size() == (size_t)L->n_d;
+    for (int r = 0; same && r < L->n_d; ++r) same = R->released_grads[r] == a->grad_replicas[r];
     cudaEvent_t gate = R->released;
-    if (!(a->overlap_previous && prev_released && !capturing)) {
+    if (!(a->overlap_previous && same && !capturing)) {
         if ((e = cudaEventRecord(R->start, s)) != cudaSuccess) return cuda_fail("zero_step_from_host: record", e);
         gate = R->start;
     }
@@ -548,6 +555,8 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
         e = cudaMemcpyAsync(host_state, a->state, sizeof(zero_step_state), cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail("zero_step_from_host: state read-back", e);
     }
+    R->released_stream = s;
+    R->released_grads.assign(a->grad_replicas, a->grad_replicas + L->n_d);
     R->released_ok = !capturing;
     return ZERO_OK;
 }

@@ -151,6 +151,9 @@ class ZeroStep:
 
     # -- initialisation (plumbing, not part of the step) -------------------------
     def reset_state(self):
+        # after the work on the current stream (the buffers' zero fill, at construction), when
+        # the engine runs on a stream of its own
+        self._s().wait_stream(torch.cuda.current_stream(self.device))
         B.zero_state_init(self.state, self.adamw.beta1, self.adamw.beta2, self.loss_scale0, self.dynamic,
                           self.growth_interval, self._s())
 
@@ -171,6 +174,7 @@ class ZeroStep:
         self.m.zero_()
         self.v.zero_()
         s = self._s()
+        s.wait_stream(torch.cuda.current_stream(self.device))   # the copies above ran on the current stream
         if self.shard16 is not None:
             B.zero_cast_params(self.L, self.master_rows, self.shard16_rows, B.ZERO_OUT_SHARDS, s)
         if self.params is not None:
@@ -457,9 +461,11 @@ class ZeroStep:
                 self.v[r].copy_(torch.from_numpy(host[2]))
                 p16_rows[r].view(torch.int16).copy_(torch.from_numpy(host[3].view(np.int16)))
         self.state.copy_(torch.frombuffer(bytearray(st), dtype=torch.uint8))
+        self._s().wait_stream(torch.cuda.current_stream(self.device))   # the uploads ran on the current stream
         if self.stage != 3:
             if self.shard16 is None:
                 shards = torch.stack([t.clone() for t in p16_rows])
+                self._s().wait_stream(torch.cuda.current_stream(self.device))
                 B.zero_allgather_params(self.L, [shards[r] for r in range(self.n_d)], self.param_rows, self._s())
                 torch.cuda.synchronize(self.device)
                 del shards
