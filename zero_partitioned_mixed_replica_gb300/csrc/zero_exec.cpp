@@ -21,7 +21,9 @@
 // own copies: later buckets cross the host link while earlier ones are
 // reduced.  This is the bucketed overlap of the reading notes §4.1-§4.2 (a
 // bucket's reduce-scatter starts as soon as backward has filled it), with the
-// host link standing in for backward.
+// host link standing in for backward.  With overlap_previous, consecutive
+// host-input steps also overlap: a step's copies wait only for the previous
+// step's last replica-reading launch, not for its norm and update.
 #include <cuda_runtime.h>
 
 #include <algorithm>
