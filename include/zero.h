@@ -590,6 +590,28 @@ const char* zero_last_error(void);
  * last reset (for launch accounting in benchmarks). */
 int64_t zero_launch_count(int32_t reset);
 
+/* Bounds-checked builds.  A build compiled with -DZK_CHECKED (the build
+ * script's checked=True, libzero_checked.so) tests every global access of
+ * every kernel against the extent the layout gives its buffer (16-bit
+ * replicas and accumulators: Psi_pad elements; fp32 shards and 16-bit
+ * shards: S; a ZeRO-3 transient: the unit's real size; norm partials:
+ * Psi_pad / 32; a rank index: N_d).  An access outside is skipped, never
+ * made, and counted; nothing traps.  This stands in for a memory checker
+ * ("the kernel reads and writes only inside the buffers the header
+ * promises").  The normal build compiles the checks out.
+ *   zero_checked_build: 1 for a checked build, 0 otherwise.
+ *   zero_bounds_violations: *count = accesses skipped on the current device
+ *     since the last reset (0 in a normal build); reset != 0 zeroes the count.
+ *     Synchronises the device.  ZERO_ERR_CUDA if reading the count fails.
+ *   zero_checked_set_slack: a test hook of checked builds: every extent the
+ *     launches check against is `elems` elements short of the real one, so
+ *     the last accesses of each buffer are reported and skipped while the
+ *     buffers stay whole.  elems >= 0; returns ZERO_ERR_STATE in a normal
+ *     build. */
+int32_t zero_checked_build(void);
+zero_status_t zero_bounds_violations(int64_t* count, int32_t reset);
+zero_status_t zero_checked_set_slack(int64_t elems);
+
 #ifdef __cplusplus
 }
 #endif

@@ -272,3 +272,16 @@ def test_unit_hook_trampoline_keeps_the_first_exception():
     B._raise_hook_error(a)                              # cleared once raised
     a.set_unit_hook(None)
     assert not a.args.unit_hook
+
+
+def test_normal_build_reports_no_checks():
+    # the bounds checks are compiled out of the normal build: it says so, counts nothing and
+    # refuses the checked build's test hook
+    if os.environ.get("ZERO_LIB"):
+        pytest.skip("another build of the library is loaded")
+    assert not B.zero_checked_build()
+    assert B.zero_bounds_violations() == 0
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_checked_set_slack(8)
+    assert e.value.status == B.ZERO_ERR_STATE
+    assert B.lib().zero_bounds_violations(None, 0) == B.ZERO_ERR_INVALID

@@ -16,7 +16,9 @@ import os
 from typing import Optional, Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libzero.so")
+# ZERO_LIB names another build of the library to load (the bounds-checked
+# libzero_checked.so); the in-tree libzero.so otherwise.
+LIB_PATH = os.environ.get("ZERO_LIB") or os.path.join(PKG, "libzero.so")
 
 ZERO_OK = 0
 ZERO_ERR_INVALID = -1
@@ -40,7 +42,8 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
             "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_micro_step", "zero_step_from_host",
             "zero_trace_enable", "zero_trace_read", "zero_set_max_ctas",
-            "zero_last_error", "zero_launch_count"]
+            "zero_last_error", "zero_launch_count", "zero_checked_build", "zero_bounds_violations",
+            "zero_checked_set_slack"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
 
 
@@ -188,6 +191,9 @@ def lib():
         "zero_step_from_host": [P, ctypes.POINTER(zero_step_args), PP, i64, P, P],
         "zero_micro_step": [P, ctypes.POINTER(zero_step_args), i32, i32, PP, P],
         "zero_trace_read": [ctypes.POINTER(zero_trace_totals), i32],
+        "zero_bounds_violations": [ctypes.POINTER(i64), i32],
+        "zero_checked_set_slack": [i64],
+        "zero_checked_build": [],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -438,3 +444,22 @@ def zero_last_error() -> str:
 
 def zero_launch_count(reset: bool = False) -> int:
     return int(lib().zero_launch_count(int(reset)))
+
+
+def zero_checked_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().zero_checked_build())
+
+
+def zero_bounds_violations(reset: bool = False) -> int:
+    """Accesses the bounds-checked build skipped on the current device (0 in
+    a normal build); synchronises the device."""
+    n = ctypes.c_int64(0)
+    _check(lib().zero_bounds_violations(ctypes.byref(n), int(reset)))
+    return int(n.value)
+
+
+def zero_checked_set_slack(elems: int) -> None:
+    """Test hook of the bounds-checked build: every checked extent is
+    ``elems`` short of the real one."""
+    _check(lib().zero_checked_set_slack(int(elems)))

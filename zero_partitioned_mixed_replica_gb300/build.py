@@ -3,7 +3,9 @@
 Each translation unit under ``csrc/`` is compiled by nvcc in parallel, then
 linked into ``zero_partitioned_mixed_replica_gb300/libzero.so`` with the CUDA
 runtime linked statically.  ``python -m zero_partitioned_mixed_replica_gb300.build``
-or :func:`build` from Python.
+or :func:`build` from Python.  ``build(checked=True)`` (or ``--checked``)
+builds the bounds-checked variant, ``libzero_checked.so``: the same sources
+with -DZK_CHECKED, objects kept apart.
 """
 from __future__ import annotations
 
@@ -19,6 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero.so")
+OBJ_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libzero_checked.so")
 
 SOURCES = ["zero_layout.cpp", "zero_rs.cu", "zero_adamw.cu", "zero_norm.cu", "zero_gather.cu",
            "zero_noalloc.cu", "zero_accum.cu", "zero_exec.cpp"]
@@ -46,18 +50,19 @@ def _newer(target: str, deps) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    obj_dir, lib = (OBJ_CHECKED, LIB_CHECKED) if checked else (OBJ, LIB)
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "zero.h")]
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src + ".o")
+        o = os.path.join(obj_dir, src + ".o")
         objs.append(o)
         if force or not _newer(o, [s] + hdrs):
-            flags = list(NVCC_FLAGS)
+            flags = list(NVCC_FLAGS) + (["-DZK_CHECKED"] if checked else [])
             if verbose_ptxas and src.endswith(".cu"):
                 flags += ["-Xptxas", "-v"]
             jobs.append([nvcc, *flags, "-c", s, "-o", o])
@@ -75,12 +80,12 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if force or jobs or not _newer(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or jobs or not _newer(lib, objs):
+        tmp = lib + ".tmp%d" % os.getpid()
         subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kThreads) accum_kernel(const __grid_constant__
         const uint32_t r = (uint32_t)(t / a.v_per_rank);
         const uint32_t v = (uint32_t)(t - (uint64_t)r * a.v_per_rank);
         const int64_t i0 = (int64_t)v * kVec;
+        if (!(in_bounds(r + 1, a.bnd.nd) && in_bounds((uint64_t)i0 + kVec, a.bnd.rep))) continue;
         float x[8];
         if (i0 + kVec <= a.real_end) {
             unpack8<F>(ld_stream(a.rep[r] + i0), x);
@@ -53,7 +54,11 @@ __global__ void __launch_bounds__(kThreads) rs_acc_kernel(const __grid_constant_
         float g[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) g[e] = 0.0f;
-        if (active) {
+        const uint32_t k = v - a.seg.seg_v;
+        const uint32_t r = k / a.seg.shard_v;
+        const uint32_t j = a.seg.base_v + (k - r * a.seg.shard_v);
+        if (active && in_bounds((uint64_t)(v + 1) * kVec, a.bnd.rep) && in_bounds(r + 1, a.bnd.nd) &&
+            in_bounds((uint64_t)(j + 1) * kVec, a.bnd.shard)) {
             const size_t i0 = (size_t)v * kVec;
             float s[8];
             ld8(a.acc[0] + i0, s);
@@ -73,13 +78,10 @@ __global__ void __launch_bounds__(kThreads) rs_acc_kernel(const __grid_constant_
                 bad |= !isfinite(s[e]);
                 g[e] = div_rn(s[e], D);
             }
-            const uint32_t k = v - a.seg.seg_v;
-            const uint32_t r = k / a.seg.shard_v;
-            const uint32_t j = a.seg.base_v + (k - r * a.seg.shard_v);
             st8(a.gshard[r] + (size_t)j * kVec, g);
         }
         const float part = group32_sumsq(g);
-        if (active && (lane & 3u) == 0u) a.partials[v >> 2] = part;
+        if (active && (lane & 3u) == 0u && in_bounds((v >> 2) + 1, a.bnd.part)) a.partials[v >> 2] = part;
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0u) atomicOr(&a.st->nonfinite, 1);
 }
@@ -106,6 +108,7 @@ extern "C" zero_status_t zero_accumulate_grads(const zero_layout* L, int32_t mic
     a.v_per_rank = (uint32_t)(L->psi_pad / zk::kVec);
     a.real_end = L->segs[0].offset + L->segs[0].real;
     a.nd = L->n_d;
+    a.bnd = make_bounds(L, 0);
     const int64_t work = ((int64_t)a.v_per_rank * a.nd + zk::kThreads - 1) / zk::kThreads;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (L->dtype == ZERO_BF16) {
@@ -150,6 +153,7 @@ extern "C" zero_status_t zero_reduce_scatter_accumulated(const zero_layout* L, i
     a.st = st;
     a.nd = L->n_d;
     a.n_micro = n_micro;
+    a.bnd = make_bounds(L, 0);
     const auto& bk = L->buckets[bucket];
     a.seg = seg_args(L->segs[L->bucket_seg[bucket]], bk.first, bk.second);
     const int64_t nvec = (bk.second - bk.first) / zk::kVec;

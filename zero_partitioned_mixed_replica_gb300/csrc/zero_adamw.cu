@@ -80,12 +80,17 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     const bool has_last = mine > 0 && c + (mine - 1) * G == nbatch - 1;  // the short batch is a CTA's last
     const uint32_t count = mine * kBatch - (has_last ? nbatch * kBatch - total : 0u);
 
+    // A tile whose extents fail the checked build's bounds test is processed
+    // as empty (len 0): nothing is loaded or stored for it.
     auto tile_of = [&](uint32_t kk, uint32_t& r, uint64_t& j0, uint32_t& len) {
         const uint32_t T = (c + (kk / kBatch) * G) * kBatch + kk % kBatch;
         r = T / ntile;
         j0 = (uint64_t)(T - r * ntile) * TE;
         const uint64_t rem = S - j0;
         len = rem < (uint64_t)TE ? (uint32_t)rem : (uint32_t)TE;
+        const uint64_t out_end = OUT == ZERO_OUT_FULL_REPLICAS ? (uint64_t)r * S + j0 + len : j0 + len;
+        if (!(in_bounds(r + 1, a.bnd.nd) && in_bounds(j0 + len, a.bnd.shard) && in_bounds(out_end, a.bnd.out)))
+            len = 0;
     };
     auto issue = [&](uint32_t kk) {  // one thread
         uint32_t r, len;
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
         float* dst = in + (size_t)slot * 4 * TE;
         const uint32_t bytes = len * (uint32_t)sizeof(float);
         mbar_arrive_expect_tx(&full[slot], 4u * bytes);
+        if (kChecked && len == 0) return;
         bulk_g2s(dst, a.gshard[r] + j0, bytes, &full[slot]);
         bulk_g2s(dst + TE, a.master[r] + j0, bytes, &full[slot]);
         bulk_g2s(dst + 2 * TE, a.m[r] + j0, bytes, &full[slot]);
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
         fence_proxy_async_smem();
         __syncthreads();
         if (s_abort) break;
-        if (tid == 0) {
+        if (tid == 0 && (!kChecked || len != 0)) {
             const uint32_t fb = len * (uint32_t)sizeof(float);
             const uint32_t hbytes = len * (uint32_t)sizeof(uint16_t);
             bulk_s2g(a.master[r] + j0, dst, fb);
@@ -211,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, 4) adamw_ldg_kernel(const __grid_con
         const uint32_t r = v / a.shard_v;
         const uint32_t j = v - r * a.shard_v;
         const size_t o = (size_t)j * kVec;
+        const uint64_t out_end = OUT == ZERO_OUT_FULL_REPLICAS ? (uint64_t)(v + 1) * kVec : o + kVec;
+        if (!(in_bounds(r + 1, a.bnd.nd) && in_bounds(o + kVec, a.bnd.shard) && in_bounds(out_end, a.bnd.out)))
+            continue;
         float g[8], p[8], m[8], w[8];
         ld8(a.gshard[r] + o, g);
         ld8(a.master[r] + o, p);
@@ -261,7 +270,13 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constan
         float g[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) g[e] = 0.0f;
-        if (active) {
+        const uint32_t kk = v - a.seg.seg_v;
+        const uint32_t r = kk / a.seg.shard_v;
+        const uint32_t j = a.seg.base_v + (kk - r * a.seg.shard_v);
+        const size_t o = (size_t)j * kVec;
+        const uint64_t out_end = OUT == ZERO_OUT_FULL_REPLICAS ? (uint64_t)(v + 1) * kVec : o + kVec;
+        if (active && in_bounds((uint64_t)(v + 1) * kVec, a.bnd.rep) && in_bounds(r + 1, a.bnd.nd) &&
+            in_bounds(o + kVec, a.bnd.shard) && in_bounds(out_end, a.bnd.out)) {
             float s[8];
             reduce8<ND, F>(a.rep, nd, v, a.seg.real_end, s);
 #pragma unroll
@@ -269,10 +284,6 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constan
                 bad |= !isfinite(s[e]);
                 g[e] = div_rn(s[e], D);
             }
-            const uint32_t kk = v - a.seg.seg_v;
-            const uint32_t r = kk / a.seg.shard_v;
-            const uint32_t j = a.seg.base_v + (kk - r * a.seg.shard_v);
-            const size_t o = (size_t)j * kVec;
             float p[8], m[8], w[8];
             ld8(a.master[r] + o, p);
             ld8(a.m[r] + o, m);
@@ -301,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_kernel(const __grid_constan
             }
         }
         const float part = group32_sumsq(g);
-        if (active && (lane & 3u) == 0u) a.partials[v >> 2] = part;
+        if (active && (lane & 3u) == 0u && in_bounds((v >> 2) + 1, a.bnd.part)) a.partials[v >> 2] = part;
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0u) atomicOr(&a.st->nonfinite, 1);
 }
@@ -463,6 +474,7 @@ extern "C" zero_status_t zero_adamw_shard_step(const zero_layout* L, const zero_
     a.shard_v = (uint32_t)(L->shard_len / zk::kVec);
     a.total_v = (uint32_t)((int64_t)nd * (L->shard_len / zk::kVec));
     a.nd = nd;
+    a.bnd = make_bounds(L, out_kind == ZERO_OUT_FULL_REPLICAS ? L->psi_pad : L->shard_len);
     if (a.total_v == 0) return ZERO_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ZK_DISPATCH(nd, L->dtype, return launch_adamw<ND, F>(a, out_kind, s));
@@ -521,6 +533,7 @@ extern "C" zero_status_t zero_fused_step(const zero_layout* L, int32_t bucket_or
         seg = L->bucket_seg[bucket_or_unit];
     }
     a.seg = seg_args(L->segs[seg], begin, end);
+    a.bnd = make_bounds(L, out_kind == ZERO_OUT_FULL_REPLICAS ? L->psi_pad : L->shard_len);
     const int64_t nvec = (end - begin) / zk::kVec;
     if (nvec == 0) return ZERO_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -19,6 +19,43 @@ constexpr int kThreads = 256;      // threads per CTA of the streaming kernels
 constexpr int kVec = 8;            // 16-bit elements per 16-byte vector
 constexpr int kMaxRanks = ZERO_MAX_RANKS;
 
+// Extents (elements) of the buffers a launch touches, from the layout; the
+// bounds-checked build tests every global access against them.
+struct Bounds {
+    uint64_t rep;    // each 16-bit gradient replica or fp32 accumulator: Psi_pad
+    uint64_t shard;  // each fp32 shard (master, m, v, reduced gradient): S
+    uint64_t out;    // each 16-bit output: Psi_pad, S, or a transient's unit size
+    uint64_t part;   // norm partials: Psi_pad / 32
+    uint64_t src;    // each 16-bit shard a gather reads: S
+    uint32_t nd;     // rank index bound
+    uint32_t pad0;
+};
+
+#ifdef ZK_CHECKED
+constexpr bool kChecked = true;
+// Accesses skipped by the checks, one counter per translation unit (the host
+// sums them, zero_bounds_violations).
+static __device__ unsigned long long zk_bounds_hits;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// True if [.., end) lies inside an extent of `lim` elements.  The checked
+// build counts and reports a miss (the caller skips the access); the normal
+// build compiles to `true`.
+__device__ __forceinline__ bool in_bounds(uint64_t end, uint64_t lim) {
+#ifdef ZK_CHECKED
+    if (end > lim) {
+        atomicAdd(&zk_bounds_hits, 1ull);
+        return false;
+    }
+#else
+    (void)end;
+    (void)lim;
+#endif
+    return true;
+}
+
 // ----------------------------------------------------------------------------
 // 16-bit formats
 // ----------------------------------------------------------------------------
@@ -419,6 +456,7 @@ struct RsArgs {
     float* partials;
     zero_step_state* st;
     SegArgs seg;
+    Bounds bnd;
     int32_t nd;
     int32_t n_micro;  // micro-batches of the step (1: plain reduce-scatter)
 };
@@ -430,6 +468,7 @@ enum { RS_PLAIN = 0, RS_FIRST = 1, RS_MIDDLE = 2, RS_LAST = 3 };
 struct AccumArgs {
     const uint16_t* rep[kMaxRanks];
     float* acc[kMaxRanks];
+    Bounds bnd;
     uint32_t v_per_rank;  // Psi_pad / 8
     int64_t real_end;     // padding starts here
     int32_t nd;
@@ -441,6 +480,7 @@ struct RsAccArgs {
     float* partials;
     zero_step_state* st;
     SegArgs seg;
+    Bounds bnd;
     int32_t nd;
     int32_t n_micro;
 };
@@ -452,6 +492,7 @@ struct AdamArgs {
     const float* gshard[kMaxRanks];
     uint16_t* out[kMaxRanks];
     zero_step_state* st;
+    Bounds bnd;
     double lr, eps, wd;
     uint32_t shard_v;   // per-rank shard length / 8
     uint32_t total_v;   // nd * shard_v
@@ -466,6 +507,7 @@ struct FusedArgs {
     uint16_t* out[kMaxRanks];
     float* partials;
     zero_step_state* st;
+    Bounds bnd;
     double lr, eps, wd;
     SegArgs seg;
     int32_t nd;
@@ -474,6 +516,7 @@ struct FusedArgs {
 struct GatherArgs {
     const uint16_t* src[kMaxRanks];
     uint16_t* dst[kMaxRanks];
+    Bounds bnd;
     uint32_t shard_v;   // S_u / 8
     uint32_t base_v;    // shard_base / 8
     int64_t n_elems;    // elements per destination (real_u, or Psi_pad)

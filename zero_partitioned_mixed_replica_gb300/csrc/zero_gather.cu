@@ -19,6 +19,10 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
         const uint32_t r = v / a.shard_v;
         const size_t so = ((size_t)a.base_v + (v - r * a.shard_v)) * kVec;
         const int64_t i0 = (int64_t)v * kVec;
+        const int64_t i1 = i0 + kVec <= a.n_elems ? i0 + kVec : a.n_elems;
+        if (!(in_bounds(r + 1, a.bnd.nd) && in_bounds(so + (uint64_t)(i1 - i0), a.bnd.src) &&
+              in_bounds((uint64_t)i1, a.bnd.out)))
+            continue;
         if (i0 + kVec <= a.n_elems) {
             const uint4 x = ld_stream(a.src[r] + so);
             if constexpr (ND > 0) {
@@ -40,6 +44,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
 struct CastArgs {
     const float* master[kMaxRanks];
     uint16_t* out[kMaxRanks];
+    Bounds bnd;
     uint32_t shard_v;  // per-rank shard length / 8
     uint32_t total_v;  // nd * shard_v
     int32_t nd;
@@ -56,6 +61,9 @@ __global__ void __launch_bounds__(kThreads) cast_kernel(const __grid_constant__ 
     for (uint32_t v = blockIdx.x * kThreads + threadIdx.x; v < a.total_v; v += gridDim.x * kThreads) {
         const uint32_t r = v / a.shard_v;
         const size_t o = (size_t)(v - r * a.shard_v) * kVec;
+        const uint64_t out_end = OUT == ZERO_OUT_FULL_REPLICAS ? (uint64_t)(v + 1) * kVec : o + kVec;
+        if (!(in_bounds(r + 1, a.bnd.nd) && in_bounds(o + kVec, a.bnd.shard) && in_bounds(out_end, a.bnd.out)))
+            continue;
         float p[8];
         ld8(a.master[r] + o, p);
         const uint4 h = pack8<F>(p);
@@ -111,6 +119,7 @@ extern "C" zero_status_t zero_cast_params(const zero_layout* L, const float* con
     a.shard_v = (uint32_t)(L->shard_len / zk::kVec);
     a.total_v = (uint32_t)((int64_t)L->n_d * (L->shard_len / zk::kVec));
     a.nd = L->n_d;
+    a.bnd = make_bounds(L, out_kind == ZERO_OUT_FULL_REPLICAS ? L->psi_pad : L->shard_len);
     if (a.total_v == 0) return ZERO_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ZK_DISPATCH(L->n_d, L->dtype, return launch_cast<ND, F>(a, out_kind, s));
@@ -164,6 +173,7 @@ extern "C" zero_status_t zero_allgather_params(const zero_layout* L, const void*
     a.base_v = 0;
     a.n_elems = L->psi_pad;
     a.nd = L->n_d;
+    a.bnd = make_bounds(L, L->psi_pad);
     return dispatch_gather(L->n_d, a, "zero_allgather_params", reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -189,5 +199,6 @@ extern "C" zero_status_t zero_stage3_gather_layer(const zero_layout* L, int32_t 
     a.base_v = (uint32_t)(sg.shard_base / zk::kVec);
     a.n_elems = sg.real;
     a.nd = L->n_d;
+    a.bnd = make_bounds(L, sg.real);   // a transient holds at least the unit's real size
     return dispatch_gather(L->n_d, a, "zero_stage3_gather_layer", reinterpret_cast<cudaStream_t>(stream));
 }

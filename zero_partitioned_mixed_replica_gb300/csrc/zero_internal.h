@@ -41,4 +41,10 @@ zero_status_t fail(zero_status_t code, const std::string& msg);
 void clear_error();
 void count_launches(int64_t n);
 int32_t max_ctas();
+// Bounds-checked builds: each CUDA translation unit registers a reader of its
+// device counter of skipped accesses (adds it to *out; reset zeroes it), and
+// the launches shorten every extent by check_slack() elements (a test hook).
+using BoundsReader = int (*)(int64_t* out, bool reset);
+void register_bounds_reader(BoundsReader fn);
+int64_t check_slack();
 }  // namespace zero_detail

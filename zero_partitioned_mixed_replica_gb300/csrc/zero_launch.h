@@ -82,6 +82,22 @@ inline zero_status_t after_launch(const char* what) {
     return ZERO_OK;
 }
 
+// The extents a launch's accesses are checked against (bounds-checked
+// builds; the normal build carries them unused): from the layout, each
+// shortened by the test hook's slack.  out_elems: each 16-bit output's size.
+inline zk::Bounds make_bounds(const zero_layout* L, int64_t out_elems) {
+    const int64_t sl = check_slack();
+    auto cut = [sl](int64_t x) { return (uint64_t)(x > sl ? x - sl : 0); };
+    zk::Bounds b{};
+    b.rep = cut(L->psi_pad);
+    b.shard = cut(L->shard_len);
+    b.out = cut(out_elems);
+    b.part = cut(partials_count(L));
+    b.src = cut(L->shard_len);
+    b.nd = (uint32_t)L->n_d;
+    return b;
+}
+
 inline zk::SegArgs seg_args(const zero_segment& s, int64_t begin, int64_t end) {
     zk::SegArgs a;
     a.v_begin = (uint32_t)(begin / zk::kVec);
@@ -95,6 +111,25 @@ inline zk::SegArgs seg_args(const zero_segment& s, int64_t begin, int64_t end) {
 }
 
 }  // namespace zero_detail
+
+#ifdef ZK_CHECKED
+// This translation unit's counter of skipped accesses, read through the
+// registry (zero_bounds_violations).
+namespace {
+int zk_read_bounds_hits(int64_t* out, bool reset) {
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned long long v = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, zk::zk_bounds_hits, sizeof v);
+    if (e == cudaSuccess && reset) {
+        const unsigned long long z = 0;
+        e = cudaMemcpyToSymbol(zk::zk_bounds_hits, &z, sizeof z);
+    }
+    *out += (int64_t)v;
+    return e == cudaSuccess ? 0 : 1;
+}
+const bool zk_bounds_registered = (zero_detail::register_bounds_reader(&zk_read_bounds_hits), true);
+}  // namespace
+#endif
 
 #define ZK_ND_SWITCH(nd, ...)                                  \
     switch (nd) {                                              \

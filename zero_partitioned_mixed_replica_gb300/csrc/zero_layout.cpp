@@ -11,7 +11,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "zero_internal.h"
 
@@ -59,6 +61,59 @@ extern "C" int64_t zero_launch_count(int32_t reset) {
     int64_t n = g_launches;
     if (reset) g_launches = 0;
     return n;
+}
+
+// ---------------------------------------------------------------------------
+// Bounds-checked builds (-DZK_CHECKED): the registry of per-translation-unit
+// counters and the extent slack of the test hook.
+// ---------------------------------------------------------------------------
+namespace zero_detail {
+static std::mutex& bounds_mu() {
+    static std::mutex mu;
+    return mu;
+}
+static std::vector<BoundsReader>& bounds_readers() {
+    static std::vector<BoundsReader> v;
+    return v;
+}
+void register_bounds_reader(BoundsReader fn) {
+    std::lock_guard<std::mutex> lock(bounds_mu());
+    bounds_readers().push_back(fn);
+}
+static std::atomic<int64_t> g_check_slack{0};
+int64_t check_slack() { return g_check_slack.load(std::memory_order_relaxed); }
+}  // namespace zero_detail
+
+extern "C" int32_t zero_checked_build(void) {
+#ifdef ZK_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+extern "C" zero_status_t zero_bounds_violations(int64_t* count, int32_t reset) {
+    clear_error();
+    if (!count) return fail(ZERO_ERR_INVALID, "zero_bounds_violations: NULL output");
+    *count = 0;
+    std::lock_guard<std::mutex> lock(bounds_mu());
+    for (BoundsReader fn : bounds_readers()) {
+        const int e = fn(count, reset != 0);
+        if (e != 0) return fail(ZERO_ERR_CUDA, "zero_bounds_violations: reading a device counter failed");
+    }
+    return ZERO_OK;
+}
+
+extern "C" zero_status_t zero_checked_set_slack(int64_t elems) {
+    clear_error();
+#ifdef ZK_CHECKED
+    if (elems < 0) return fail(ZERO_ERR_INVALID, "zero_checked_set_slack: elems must be >= 0");
+    g_check_slack.store(elems, std::memory_order_relaxed);
+    return ZERO_OK;
+#else
+    (void)elems;
+    return fail(ZERO_ERR_STATE, "zero_checked_set_slack: not a bounds-checked build");
+#endif
 }
 
 extern "C" zero_status_t zero_layout_init(const int64_t* numels, int32_t n_tensors,

@@ -60,12 +60,13 @@ __device__ __forceinline__ void rs_body(const RsArgs& a) {
         float g[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) g[e] = 0.0f;
-        if (active) {
+        const uint32_t k = v - a.seg.seg_v;
+        const uint32_t r = k / a.seg.shard_v;
+        const uint32_t j = a.seg.base_v + (k - r * a.seg.shard_v);
+        if (active && in_bounds((uint64_t)(v + 1) * kVec, a.bnd.rep) && in_bounds(r + 1, a.bnd.nd) &&
+            in_bounds((uint64_t)(j + 1) * kVec, a.bnd.shard)) {
             float s[8];
             reduce8<ND, F>(a.rep, nd, v, a.seg.real_end, s);
-            const uint32_t k = v - a.seg.seg_v;
-            const uint32_t r = k / a.seg.shard_v;
-            const uint32_t j = a.seg.base_v + (k - r * a.seg.shard_v);
             float* dst = a.gshard[r] + (size_t)j * kVec;
             rs_combine<MODE>(s, dst, D, bad);
 #pragma unroll
@@ -74,7 +75,7 @@ __device__ __forceinline__ void rs_body(const RsArgs& a) {
         }
         if constexpr (MODE == RS_PLAIN || MODE == RS_LAST) {
             const float part = group32_sumsq(g);
-            if (active && (lane & 3u) == 0u) a.partials[v >> 2] = part;
+            if (active && (lane & 3u) == 0u && in_bounds((v >> 2) + 1, a.bnd.part)) a.partials[v >> 2] = part;
         }
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0u) atomicOr(&a.st->nonfinite, 1);
@@ -102,12 +103,13 @@ __global__ void __launch_bounds__(kThreads) rs16_kernel(const __grid_constant__ 
         float g[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) g[e] = 0.0f;
-        if (active) {
+        const uint32_t k = v - seg16;
+        const uint32_t r = k / sh16;
+        const uint32_t j = base16 + (k - r * sh16);
+        if (active && in_bounds((uint64_t)(v + 1) * 16, a.bnd.rep) && in_bounds(r + 1, a.bnd.nd) &&
+            in_bounds((uint64_t)(j + 1) * 16, a.bnd.shard)) {
             float s[16];
             reduce16<ND, F>(a.rep, v, a.seg.real_end, s);
-            const uint32_t k = v - seg16;
-            const uint32_t r = k / sh16;
-            const uint32_t j = base16 + (k - r * sh16);
             float* dst = a.gshard[r] + (size_t)j * 16;
             float* h0 = reinterpret_cast<float*>(&s[0]);
             rs_combine<MODE>(*reinterpret_cast<float(*)[8]>(h0), dst, D, bad);
@@ -122,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) rs16_kernel(const __grid_constant__ 
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc_sq(g[e], hi, lo);
             combine_lanes(hi, lo, 1);
-            if (active && (lane & 1u) == 0u) a.partials[v >> 1] = __fadd_rn(hi, lo);
+            if (active && (lane & 1u) == 0u && in_bounds((v >> 1) + 1, a.bnd.part))
+                a.partials[v >> 1] = __fadd_rn(hi, lo);
         }
     }
     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0u) atomicOr(&a.st->nonfinite, 1);
@@ -174,6 +177,7 @@ static zero_status_t rs_common(const zero_layout* L, int32_t bucket_or_unit, con
     a.st = st;
     a.nd = L->n_d;
     a.n_micro = n_micro;
+    a.bnd = make_bounds(L, 0);
     const auto& bk = L->buckets[bucket_or_unit];
     a.seg = seg_args(L->segs[L->bucket_seg[bucket_or_unit]], bk.first, bk.second);
     const int64_t nvec = (bk.second - bk.first) / zk::kVec;
