@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.step import AdamWHP, FMT_BF16, FMT_FP16, StepState, ZeroSimulation
+from oracle.step import AdamWHP, FMT_BF16, FMT_FP16, ZeroSimulation
 from tests._cases import Case
 
 pytestmark = pytest.mark.gpu

@@ -3,7 +3,6 @@ a larger allocation whose guard bands (before and after, 256-byte aligned)
 hold a sentinel pattern; after several steps of every kind of launch the
 guards must be untouched.  Shapes are ragged (odd tensor sizes, buckets that
 straddle shards, units of different sizes)."""
-import numpy as np
 import pytest
 import torch
 

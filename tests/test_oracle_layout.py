@@ -1,7 +1,5 @@
 """Oracle pins: the flat layout by brute force on tiny inputs, and the model
 parameter counts of the workloads (public figures of the named models)."""
-import itertools
-
 import pytest
 
 from oracle.layout import make_layout
