@@ -65,6 +65,9 @@ def parse():
     p.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     p.add_argument("--whole-buffer", action="store_true",
                    help="fused path: one launch over the whole buffer instead of one per bucket")
+    p.add_argument("--timeline", default="",
+                   help="write every traced call of the timed steps as a Chrome trace (JSON) to this path, "
+                        "and add launch-gap and overlap figures to the line")
     p.add_argument("--sweep", action="store_true",
                    help="350M+1 layout: GB/s vs bucket size and N_d for stages 1/2/3 (one JSON line per point)")
     p.add_argument("--sweep-nd", default="2,4,8,16,64")
@@ -360,6 +363,46 @@ def default_cpu_blocks(w) -> int:
 # GPU run
 # ---------------------------------------------------------------------------
 
+def timeline_summary(records) -> dict:
+    """Launch gaps and overlap of a traced timeline (one device): the span
+    from the first start to the last end, the time with at least one call in
+    flight (busy), the idle gaps between calls, and how many calls started
+    before the previous one (in start order) had ended."""
+    recs = sorted(records, key=lambda r: r["start_ms"])
+    if not recs:
+        return {"records": 0}
+    span = recs[-1]["end_ms"] - recs[0]["start_ms"]
+    busy, lo, hi, gaps, overlapped = 0.0, recs[0]["start_ms"], recs[0]["end_ms"], [], 0
+    for r in recs[1:]:
+        if r["start_ms"] < hi:
+            overlapped += 1
+        if r["start_ms"] > hi:
+            busy += hi - lo
+            gaps.append(r["start_ms"] - hi)
+            lo, hi = r["start_ms"], r["end_ms"]
+        else:
+            hi = max(hi, r["end_ms"])
+    busy += hi - lo
+    return {"records": len(recs), "streams": len({r["stream"] for r in recs}), "span_ms": span, "busy_ms": busy,
+            "idle_frac": 1.0 - busy / span if span > 0 else 0.0, "gaps": len(gaps),
+            "mean_gap_us": 1e3 * sum(gaps) / len(gaps) if gaps else 0.0,
+            "max_gap_us": 1e3 * max(gaps) if gaps else 0.0, "overlapped_starts": overlapped}
+
+
+def write_timeline(records, path: str) -> dict:
+    """Chrome trace (chrome://tracing, Perfetto) of the traced calls: one
+    row per stream; returns the summary with the file's path."""
+    streams = {}
+    events = []
+    for r in records:
+        tid = streams.setdefault((r["device"], r["stream"]), len(streams))
+        events.append({"name": r["kind"], "ph": "X", "pid": r["device"], "tid": tid,
+                       "ts": 1e3 * r["start_ms"], "dur": 1e3 * (r["end_ms"] - r["start_ms"])})
+    with open(path, "w") as f:
+        json.dump({"traceEvents": events, "displayTimeUnit": "ms"}, f)
+    return dict(timeline_summary(records), file=path)
+
+
 def gpu_run(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -429,8 +472,11 @@ def gpu_run(args, w, rank, world, local_rank):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     traced = None
+    timeline = None
     if trace:
         B.zero_trace_enable(False)
+        if args.timeline and rank == 0:
+            timeline = write_timeline(B.zero_trace_timeline(), args.timeline)
         traced = B.zero_trace_read(reset=True)
     ms = max_over_ranks(ms, world)
     if graph is not None:
@@ -510,7 +556,7 @@ def gpu_run(args, w, rank, world, local_rank):
             del host_grads
         except RuntimeError as ex:
             e2e = {"value": None, "unit": "params/s", "error": str(ex)[:200]}
-    return eng, info, ms, kern, launches, clk, st, e2e
+    return eng, info, ms, kern, launches, clk, st, e2e, timeline
 
 
 def sweep(args):
@@ -712,7 +758,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo", rank=rank, world_size=world)
-    eng, info, ms, kern, launches, clk, st, e2e = gpu_run(args, w, rank, world, local_rank)
+    eng, info, ms, kern, launches, clk, st, e2e, timeline = gpu_run(args, w, rank, world, local_rank)
     step_s = ms / 1e3 / args.steps
     value = world * w.psi / step_s
     step_gbs = bpp * info.psi_pad / step_s / 1e9
@@ -760,6 +806,8 @@ def main():
             "kernels": kern, "graph": bool(args.graph),
             "last_step_state": {k: st[k] for k in ("t", "skipped", "overflow", "grad_norm", "clip_coef",
                                                    "loss_scale")}}
+    if timeline is not None:
+        line["timeline"] = timeline
     print(json.dumps(line), flush=True)
 
 

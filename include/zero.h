@@ -480,6 +480,26 @@ int32_t zero_trace_enable(int32_t on);
  * query (ZERO_ERR_CUDA). */
 zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset);
 
+/* One traced call on a time axis (a timeline, for launch gaps and overlap
+ * between streams). */
+typedef struct zero_trace_record {
+    int32_t kind;                 /* ZERO_CALL_*                                 */
+    int32_t device;               /* CUDA device index                           */
+    uint64_t stream;              /* the launching stream's handle, as an id     */
+    double start_ms;              /* its first timing event, from the device's
+                                     first traced event (CUDA event resolution,
+                                     about 0.5 us)                              */
+    double end_ms;                /* its second timing event                     */
+} zero_trace_record;
+
+/* The calls traced since the last reset, in issue order.  Blocks until every
+ * recorded event has completed.  Writes min(capacity, count) records to out
+ * (out may be NULL when capacity is 0, to ask for the count) and sets *count
+ * to the number of records held.  reset != 0 clears the record afterwards,
+ * as zero_trace_read does.  Errors: NULL count, capacity < 0, or capacity > 0
+ * with a NULL out (ZERO_ERR_INVALID); a failing event query (ZERO_ERR_CUDA). */
+zero_status_t zero_trace_timeline(zero_trace_record* out, int64_t capacity, int64_t* count, int32_t reset);
+
 /* ------------------------------------------------------------------------ */
 /* Gradient accumulation over M micro-batches per optimizer step             */
 /* ------------------------------------------------------------------------ */

@@ -231,7 +231,7 @@ def test_ctypes_structs_match_the_header(tmp_path):
     structs = {"zero_step_args": B.zero_step_args, "zero_step_state": B.zero_step_state,
                "zero_trace_totals": B.zero_trace_totals, "zero_layout_info": B.zero_layout_info,
                "zero_unit_info": B.zero_unit_info, "zero_adamw_hp": B.zero_adamw_hp,
-               "zero_copy_segment": B.zero_copy_segment}
+               "zero_copy_segment": B.zero_copy_segment, "zero_trace_record": B.zero_trace_record}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "zero.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append('printf("%s %%zu\\n", sizeof(%s));' % (name, name))
@@ -285,3 +285,12 @@ def test_normal_build_reports_no_checks():
         B.zero_checked_set_slack(8)
     assert e.value.status == B.ZERO_ERR_STATE
     assert B.lib().zero_bounds_violations(None, 0) == B.ZERO_ERR_INVALID
+
+
+def test_trace_timeline_validates_and_is_empty_without_records():
+    import ctypes
+    n = ctypes.c_int64(-1)
+    assert B.lib().zero_trace_timeline(None, 0, None, 0) == B.ZERO_ERR_INVALID
+    assert B.lib().zero_trace_timeline(None, 4, ctypes.byref(n), 0) == B.ZERO_ERR_INVALID
+    assert B.lib().zero_trace_timeline(None, -1, ctypes.byref(n), 0) == B.ZERO_ERR_INVALID
+    assert B.zero_trace_timeline() == []

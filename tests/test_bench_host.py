@@ -138,3 +138,31 @@ def test_e2e_skips_when_pinned_copies_would_crowd_the_host():
     assert bench.e2e_fits(25 * gb, 2, 199 * gb)
     assert not bench.e2e_fits(25 * gb, 8, 199 * gb)      # 8 ranks would pin 200 GB
     assert bench.e2e_fits(25 * gb, 8, None)              # unknown: no guard
+
+
+def test_timeline_summary_gaps_and_overlap():
+    import bench
+    recs = [  # stream 1: 0-1 ms, stream 2: 0.5-2 ms (overlaps), gap, stream 1: 2.5-3 ms, gap, 3.2-4 ms
+        {"kind": "fused_step", "device": 0, "stream": 1, "start_ms": 0.0, "end_ms": 1.0},
+        {"kind": "fused_step", "device": 0, "stream": 2, "start_ms": 0.5, "end_ms": 2.0},
+        {"kind": "grad_norm", "device": 0, "stream": 1, "start_ms": 2.5, "end_ms": 3.0},
+        {"kind": "grad_norm", "device": 0, "stream": 1, "start_ms": 3.2, "end_ms": 4.0},
+    ]
+    s = bench.timeline_summary(list(reversed(recs)))
+    assert s["records"] == 4 and s["streams"] == 2 and s["overlapped_starts"] == 1
+    assert abs(s["span_ms"] - 4.0) < 1e-12 and abs(s["busy_ms"] - 3.3) < 1e-12
+    assert s["gaps"] == 2 and abs(s["mean_gap_us"] - 350.0) < 1e-9 and abs(s["max_gap_us"] - 500.0) < 1e-9
+    assert abs(s["idle_frac"] - 0.7 / 4.0) < 1e-12
+    assert bench.timeline_summary([]) == {"records": 0}
+
+
+def test_timeline_file_is_a_chrome_trace(tmp_path):
+    import bench
+    recs = [{"kind": "reduce_scatter", "device": 0, "stream": 77, "start_ms": 0.25, "end_ms": 1.25},
+            {"kind": "adamw", "device": 0, "stream": 78, "start_ms": 1.5, "end_ms": 3.0}]
+    out = bench.write_timeline(recs, str(tmp_path / "t.json"))
+    d = json.load(open(out["file"]))
+    ev = d["traceEvents"]
+    assert [e["name"] for e in ev] == ["reduce_scatter", "adamw"] and [e["tid"] for e in ev] == [0, 1]
+    assert ev[0]["ph"] == "X" and ev[0]["ts"] == 250.0 and ev[0]["dur"] == 1000.0
+    assert out["records"] == 2 and out["gaps"] == 1

@@ -804,3 +804,37 @@ def test_long_run_with_natural_overflows():
     assert sum(over) >= 2, over
     assert max(scales) > 65536.0 and any(b < a for a, b in zip(scales, scales[1:]))
     assert hist[-1][0]["t"] == 200 - sum(over)
+
+
+def test_trace_timeline_of_a_step():
+    # the executor's per-call timeline: one record per library call, each on the stream it was
+    # issued on; a ZeRO-1 step of short buckets spreads its bucket launches over several streams
+    from zero_partitioned_mixed_replica_gb300 import binding as Bd
+    c = Case([200_000, 1600, 99_999, 333], 8, 1, FMT_BF16, bucket_elems=32_768)
+    eng = _engine(c)
+    eng.load_master(torch.from_numpy(c.master0(c.layout())))
+    eng.step()
+    torch.cuda.synchronize()
+    Bd.zero_trace_read(reset=True)
+    Bd.zero_trace_enable(True)
+    try:
+        Bd.zero_launch_count(reset=True)
+        eng.step()
+        eng.step()
+        torch.cuda.synchronize()
+        launches = Bd.zero_launch_count()
+        tl = Bd.zero_trace_timeline()
+        totals = Bd.zero_trace_read(reset=True)
+    finally:
+        Bd.zero_trace_enable(False)
+    assert len(tl) == sum(v["launches"] for v in totals.values())     # one record per library call
+    assert {r["kind"] for r in tl} == {"fused_step", "grad_norm"}
+    assert launches == len(tl) + sum(r["kind"] == "grad_norm" for r in tl)   # the norm call is two kernels
+    assert all(r["end_ms"] >= r["start_ms"] >= 0.0 for r in tl)
+    buckets = eng.n_buckets
+    assert sum(r["kind"] == "fused_step" for r in tl) == 2 * buckets
+    assert len({r["stream"] for r in tl if r["kind"] == "fused_step"}) >= 2
+    norm = [r for r in tl if r["kind"] == "grad_norm"]
+    fused = [r for r in tl if r["kind"] == "fused_step"]
+    # each step's norm starts after that step's last bucket launch has ended (the lanes join first)
+    assert norm[0]["start_ms"] >= max(r["end_ms"] for r in fused[:buckets]) - 1e-3

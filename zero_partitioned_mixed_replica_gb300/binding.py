@@ -41,7 +41,7 @@ EXPORTED = ["zero_layout_init", "zero_layout_query", "zero_layout_bucket", "zero
             "zero_allgather_params", "zero_cast_params", "zero_stage3_gather_layer", "zero_fused_step",
             "zero_fused_step_noalloc", "zero_reshard_plan", "zero_accumulate_grads",
             "zero_reduce_scatter_accumulated", "zero_reduce_scatter_micro", "zero_step", "zero_micro_step", "zero_step_from_host",
-            "zero_trace_enable", "zero_trace_read", "zero_set_max_ctas",
+            "zero_trace_enable", "zero_trace_read", "zero_trace_timeline", "zero_set_max_ctas",
             "zero_last_error", "zero_launch_count", "zero_checked_build", "zero_bounds_violations",
             "zero_checked_set_slack"]
 ZERO_NOALLOC_MAX_ELEMS = 67108864
@@ -90,6 +90,11 @@ ZERO_CALL_NAMES = ["reduce_scatter", "grad_norm", "adamw", "fused_step", "stage3
 
 class zero_trace_totals(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_int64 * 8), ("total_ms", ctypes.c_double * 8), ("busy_ms", ctypes.c_double * 8)]
+
+
+class zero_trace_record(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("device", ctypes.c_int32), ("stream", ctypes.c_uint64),
+                ("start_ms", ctypes.c_double), ("end_ms", ctypes.c_double)]
 
 
 ZERO_UNIT_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -191,6 +196,7 @@ def lib():
         "zero_step_from_host": [P, ctypes.POINTER(zero_step_args), PP, i64, P, P],
         "zero_micro_step": [P, ctypes.POINTER(zero_step_args), i32, i32, PP, P],
         "zero_trace_read": [ctypes.POINTER(zero_trace_totals), i32],
+        "zero_trace_timeline": [ctypes.POINTER(zero_trace_record), i64, ctypes.POINTER(i64), i32],
         "zero_bounds_violations": [ctypes.POINTER(i64), i32],
         "zero_checked_set_slack": [i64],
         "zero_checked_build": [],
@@ -432,6 +438,20 @@ def zero_trace_read(reset: bool = True) -> dict:
     return {name: {"launches": int(t.calls[k]), "total_ms": float(t.total_ms[k]), "busy_ms": float(t.busy_ms[k]),
                    "avg_ms": float(t.busy_ms[k]) / int(t.calls[k])}
             for k, name in enumerate(ZERO_CALL_NAMES) if t.calls[k] > 0}
+
+
+def zero_trace_timeline(reset: bool = False) -> list:
+    """Every call traced since the last reset, in issue order:
+    [{"kind": name, "device": d, "stream": id, "start_ms": a, "end_ms": b}];
+    times on one axis per device, from its first traced event."""
+    n = ctypes.c_int64(0)
+    _check(lib().zero_trace_timeline(None, 0, ctypes.byref(n), 0))
+    buf = (zero_trace_record * max(1, n.value))()
+    _check(lib().zero_trace_timeline(buf, n.value, ctypes.byref(n), int(bool(reset))))
+    names = ZERO_CALL_NAMES
+    return [{"kind": names[r.kind] if 0 <= r.kind < len(names) else str(r.kind), "device": int(r.device),
+             "stream": int(r.stream), "start_ms": float(r.start_ms), "end_ms": float(r.end_ms)}
+            for r in buf[:min(n.value, len(buf))]]
 
 
 def zero_set_max_ctas(n: int) -> int:

@@ -105,6 +105,7 @@ constexpr size_t kTraceMaxRecords = (size_t)1 << 20;
 struct TraceRecord {
     int32_t kind;
     int32_t dev;
+    cudaStream_t stream;
     cudaEvent_t e0, e1;
 };
 std::mutex g_trace_mu;
@@ -143,7 +144,7 @@ zero_status_t traced(int32_t kind, cudaStream_t st, Call&& call) {
     const zero_status_t rc = call();
     cudaEventRecord(e1, st);
     std::lock_guard<std::mutex> lock(g_trace_mu);
-    g_trace.push_back({kind, dev, e0, e1});
+    g_trace.push_back({kind, dev, st, e0, e1});
     return rc;
 }
 
@@ -565,14 +566,13 @@ extern "C" zero_status_t zero_step_from_host(const zero_layout* L, const zero_st
 
 extern "C" int32_t zero_trace_enable(int32_t on) { return g_trace_on.exchange(on ? 1 : 0); }
 
-extern "C" zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset) {
-    clear_error();
-    if (!out) return fail(ZERO_ERR_INVALID, "zero_trace_read: NULL output");
-    *out = zero_trace_totals{};
-    std::lock_guard<std::mutex> lock(g_trace_mu);
-    // busy time per kind: the union of its calls' intervals, placed on one
-    // time axis per device by their offsets from that device's first event
-    std::vector<std::pair<double, double>> spans[ZERO_CALL_KINDS];
+namespace {
+// Start and duration (ms) of every record, on one time axis per device: the
+// offset from that device's first recorded event.  Waits for the events.
+// Call with g_trace_mu held.
+zero_status_t trace_times(std::vector<std::pair<float, float>>& times, const char* what) {
+    times.clear();
+    times.reserve(g_trace.size());
     cudaEvent_t ref[64] = {nullptr};
     for (const TraceRecord& t : g_trace) {
         cudaError_t e = cudaEventSynchronize(t.e1);
@@ -580,11 +580,39 @@ extern "C" zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset) 
         if (!ref[t.dev]) ref[t.dev] = t.e0;
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.e0, t.e1);
         if (e == cudaSuccess) e = cudaEventElapsedTime(&at, ref[t.dev], t.e0);
-        if (e != cudaSuccess) return cuda_fail("zero_trace_read", e);
+        if (e != cudaSuccess) return cuda_fail(what, e);
+        times.push_back({at, ms});
+    }
+    return ZERO_OK;
+}
+
+void trace_clear() {  // with g_trace_mu held: the events go back to the pools
+    for (const TraceRecord& t : g_trace) {
+        g_trace_free[t.dev].push_back(t.e0);
+        g_trace_free[t.dev].push_back(t.e1);
+    }
+    g_trace.clear();
+}
+}  // namespace
+
+extern "C" zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset) {
+    clear_error();
+    if (!out) return fail(ZERO_ERR_INVALID, "zero_trace_read: NULL output");
+    *out = zero_trace_totals{};
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    std::vector<std::pair<float, float>> times;
+    zero_status_t rc = trace_times(times, "zero_trace_read");
+    if (rc != ZERO_OK) return rc;
+    // busy time per kind: the union of its calls' intervals, placed on one
+    // time axis per device by their offsets from that device's first event
+    std::vector<std::pair<double, double>> spans[ZERO_CALL_KINDS];
+    for (size_t i = 0; i < g_trace.size(); ++i) {
+        const TraceRecord& t = g_trace[i];
+        const double at = times[i].first, ms = times[i].second;
         if (t.kind >= 0 && t.kind < ZERO_CALL_KINDS) {
             out->calls[t.kind] += 1;
             out->total_ms[t.kind] += ms;
-            spans[t.kind].push_back({(double)at + 1e6 * t.dev, (double)at + 1e6 * t.dev + ms});
+            spans[t.kind].push_back({at + 1e6 * t.dev, at + 1e6 * t.dev + ms});
         }
     }
     for (int k = 0; k < ZERO_CALL_KINDS; ++k) {
@@ -603,12 +631,30 @@ extern "C" zero_status_t zero_trace_read(zero_trace_totals* out, int32_t reset) 
         if (hi > lo) busy += hi - lo;
         out->busy_ms[k] = busy;
     }
-    if (reset) {
-        for (const TraceRecord& t : g_trace) {
-            g_trace_free[t.dev].push_back(t.e0);
-            g_trace_free[t.dev].push_back(t.e1);
-        }
-        g_trace.clear();
+    if (reset) trace_clear();
+    return ZERO_OK;
+}
+
+extern "C" zero_status_t zero_trace_timeline(zero_trace_record* out, int64_t capacity, int64_t* count,
+                                             int32_t reset) {
+    clear_error();
+    if (!count) return fail(ZERO_ERR_INVALID, "zero_trace_timeline: NULL count");
+    if (capacity < 0 || (capacity > 0 && !out))
+        return fail(ZERO_ERR_INVALID, "zero_trace_timeline: need capacity >= 0 and an output array");
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    std::vector<std::pair<float, float>> times;
+    zero_status_t rc = trace_times(times, "zero_trace_timeline");
+    if (rc != ZERO_OK) return rc;
+    *count = (int64_t)g_trace.size();
+    const size_t n = std::min((size_t)capacity, g_trace.size());
+    for (size_t i = 0; i < n; ++i) {
+        const TraceRecord& t = g_trace[i];
+        out[i].kind = t.kind;
+        out[i].device = t.dev;
+        out[i].stream = (uint64_t)(uintptr_t)t.stream;
+        out[i].start_ms = times[i].first;
+        out[i].end_ms = (double)times[i].first + times[i].second;
     }
+    if (reset) trace_clear();
     return ZERO_OK;
 }
