@@ -67,7 +67,8 @@ def parse():
                    help="fused path: one launch over the whole buffer instead of one per bucket")
     p.add_argument("--timeline", default="",
                    help="write every traced call of the timed steps as a Chrome trace (JSON) to this path, "
-                        "and add launch-gap and overlap figures to the line")
+                        "and add launch-gap and overlap figures to the line (eager steps only: calls replayed "
+                        "from a CUDA graph are not traced)")
     p.add_argument("--sweep", action="store_true",
                    help="350M+1 layout: GB/s vs bucket size and N_d for stages 1/2/3 (one JSON line per point)")
     p.add_argument("--sweep-nd", default="2,4,8,16,64")
