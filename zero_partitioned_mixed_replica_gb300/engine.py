@@ -488,6 +488,8 @@ class ZeroStep:
         """Reassemble master/m/v (fp32) or shard16 (ZeRO-3) into flat order."""
         src = {"master": self.master, "m": self.m, "v": self.v, "shard16": self.shard16,
                "gshard": self.gshard}[which]
+        # the copies below run on the current stream: after the engine's own stream
+        torch.cuda.current_stream(self.device).wait_stream(self._s())
         out = torch.zeros(self.info.psi_pad, dtype=src.dtype, device=src.device)
         for u in self.units:
             for r in range(self.n_d):
