@@ -300,6 +300,7 @@ class ZeroStep:
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))
+        side.wait_stream(self._s())          # and the engine's own stream, if it has one
         old = self.stream
         try:
             with torch.cuda.stream(side):
