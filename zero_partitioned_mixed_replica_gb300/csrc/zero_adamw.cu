@@ -63,27 +63,24 @@ __global__ void __launch_bounds__(NT, 1) adamw_tma_kernel(const __grid_constant_
     const uint64_t S = (uint64_t)a.shard_v * kVec;
     const uint32_t ntile = (uint32_t)((S + TE - 1) / TE);
     const uint32_t total = ntile * (uint32_t)nd;
-    // Tiles are dealt to the CTAs in batches of kBatch consecutive tiles,
-    // round-robin: CTA c takes batches c, c + G, c + 2G, ...  An element whose
-    // gradient and moments are all zero (an embedding row no batch has touched
-    // yet) sends both divisions of the update down their slow path and costs
-    // about twice a dense one; dealt this way a contiguous zero region spreads
-    // over every CTA.  GB300, 1.5B launch, dense / word-embedding gradients
-    // zero: 10.71 / 11.25 ms; one contiguous range per CTA: 10.68 / 20.91 ms
-    // (the few CTAs holding the zero region set the time); single tiles
-    // round-robin: 10.73 / 11.27; batches of 16 or 64: 10.77 or 10.87 ms
-    // dense (a batch-sized tail).
-    constexpr uint32_t kBatch = 4;
-    const uint32_t nbatch = (total + kBatch - 1) / kBatch;
+    // Tiles are dealt to the CTAs round-robin: CTA c takes tiles c, c + G,
+    // c + 2G, ...  An element whose gradient and moments are all zero (an
+    // embedding row no batch has touched yet) sends both divisions of the
+    // update down their slow path and costs about twice a dense one; dealt this
+    // way a contiguous zero region spreads over every CTA.  GB300, 1.5B launch:
+    // one contiguous range of tiles per CTA took 10.68 ms dense but 20.91 ms
+    // with the word-embedding gradients zero (the few CTAs holding the zero
+    // region set the time), round-robin 10.73 / 11.27 ms.  On the current
+    // refill schedule, single tiles against batches of 4 consecutive tiles
+    // round-robin: 10.716 / 10.750 and 10.726 / 10.762 ms (two boxes); batches
+    // of 2 or 8: 10.820, 10.790.
     const uint32_t G = gridDim.x, c = blockIdx.x;
-    const uint32_t mine = c < nbatch ? (nbatch - c + G - 1) / G : 0u;
-    const bool has_last = mine > 0 && c + (mine - 1) * G == nbatch - 1;  // the short batch is a CTA's last
-    const uint32_t count = mine * kBatch - (has_last ? nbatch * kBatch - total : 0u);
+    const uint32_t count = c < total ? (total - c + G - 1) / G : 0u;
 
     // A tile whose extents fail the checked build's bounds test is processed
     // as empty (len 0): nothing is loaded or stored for it.
     auto tile_of = [&](uint32_t kk, uint32_t& r, uint64_t& j0, uint32_t& len) {
-        const uint32_t T = (c + (kk / kBatch) * G) * kBatch + kk % kBatch;
+        const uint32_t T = c + kk * G;
         r = T / ntile;
         j0 = (uint64_t)(T - r * ntile) * TE;
         const uint64_t rem = S - j0;
